@@ -1,0 +1,183 @@
+/*
+ * inkling_rel_attn.h -- C ABI of libinkling_rel_attn.so
+ *
+ * Paged-KV, RoPE-free grouped-query attention with a learned additive
+ * relative-position bias, for one attention layer per call, on an sm_103a GPU.
+ *
+ * What is computed (Support Inkling-NVFP4 model, TensorRT-LLM PR #17062,
+ * "Architecture" and "Implementation"; Fail fast on Inkling's unsupported GPU
+ * architectures, vLLM PR #51560, "Purpose"): for a query token t at absolute
+ * position p of sequence b and query head h, with h_kv = h / (H_q / H_kv),
+ *
+ *   K_j = k_cache[page_table[b * page_table_stride + j / page_size],
+ *                 j % page_size, h_kv, :]            (V_j likewise)
+ *   key j is visible iff j <= p and (window <= 0 or p - j < window)
+ *   s_j = scale * <q[t, h, :], K_j> + rel_logits[t, h, min(p - j, R - 1)]
+ *   out[t, h, :] = sum over visible j of softmax(s)_j * V_j
+ *   lse[t, h]    = log(sum over visible j of exp(s_j))          (natural log)
+ *
+ * A query with no visible key (a sequence of length 0) gets out = 0 and
+ * lse = -inf.  The local layers of the model use window 512 with 16 KV heads,
+ * the global layers a full causal mask (window <= 0) with 8 KV heads; the
+ * bias table rel_logits has a static shape [tokens, H_q, R] (TensorRT-LLM
+ * PR #17062, "Implementation": that is what makes decode graph-capturable).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor arguments are DEVICE pointers to dense row-major arrays owned
+ *   by the caller.  The library never allocates, frees, synchronises or reads
+ *   device data on the host, so every call can be captured in a CUDA graph
+ *   once its workspace exists; device-side metadata (page_table, seq_lens,
+ *   cu_seqlens_q) may change between graph replays.
+ * - Element types: q, k_cache, v_cache, out are bf16 (raw 16-bit words);
+ *   rel_logits and lse_out are fp32; page_table, seq_lens, cu_seqlens_q int32.
+ * - Alignment: q, k_cache, v_cache, out and workspace must be 16-byte aligned;
+ *   every other pointer 4-byte aligned.
+ * - Supported shapes: D in {64, 128}; H_q % H_kv == 0 and H_q / H_kv <= 16;
+ *   page_size a multiple of 16, at most 256; R >= 1 (prefill: R % 4 == 0).
+ * - Return value: 0 on success, a negative INKLING_* code otherwise (see
+ *   inkling_rel_attn_error_string).  Validation looks at host scalars and
+ *   pointer values only.  Nothing is launched when a call fails validation.
+ * - device_error (optional, may be NULL): a device int32 word into which
+ *   kernels OR an INKLING_DEVERR_* bit when they meet bad device data (a page
+ *   id outside [0, num_pages), a sequence longer than its page-table row) or a
+ *   pipeline wait that timed out.  Kernels never trap; bad page ids read zeros.
+ *   The caller clears the word and reads it back when it chooses.
+ * - stream: the CUDA stream (cudaStream_t) everything is enqueued on.
+ */
+#ifndef INKLING_REL_ATTN_H
+#define INKLING_REL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define INKLING_OK 0
+#define INKLING_ERR_ARG (-1)        /* bad scalar, NULL required pointer, unsupported shape */
+#define INKLING_ERR_ALIGN (-2)      /* a pointer violates the alignment rule above */
+#define INKLING_ERR_WORKSPACE (-3)  /* workspace missing or smaller than required */
+#define INKLING_ERR_DEVICE (-4)     /* current device is not an sm_103 GPU */
+#define INKLING_ERR_CUDA (-5)       /* a CUDA runtime/driver call or launch failed */
+
+#define INKLING_DEVERR_BAD_PAGE 1    /* page id out of range (read as zeros) */
+#define INKLING_DEVERR_SEQ_TOO_LONG 2 /* seq_len > page_table_stride*page_size (clamped) */
+#define INKLING_DEVERR_TIMEOUT 4     /* a pipeline wait gave up; outputs are invalid */
+#define INKLING_DEVERR_BAD_CHUNK 8   /* prefill: q_len > seq_len or q_len > max_q_len */
+
+/*
+ * inkling_rel_attn_decode -- one query token per sequence.
+ *
+ * Definition: the formula above with t = b and p = seq_lens[b] - 1 (the
+ * current token's K/V are already in the cache; TensorRT-LLM PR #17062 commit
+ * notes on skip_kv_write: the attention step writes K/V before it reads them).
+ * Split-KV with a log-sum-exp merge (vLLM PR #51560, "Changes":
+ * inkling_fa4_num_splits; gist "serving Inkling-NVFP4 on 8x H200": split-KV
+ * path with num_splits=32): each sequence's visible keys are cut into up to
+ * num_splits contiguous ranges, each range is reduced to a normalised partial
+ * output and its lse, and a second kernel merges them.
+ *
+ *   q           bf16 [B, H_q, D]
+ *   k_cache     bf16 [num_pages, page_size, H_kv, D]
+ *   v_cache     bf16 [num_pages, page_size, H_kv, D]
+ *   page_table  int32 [B, page_table_stride]; row b lists sequence b's
+ *               physical pages in logical order
+ *   seq_lens    int32 [B]; keys of sequence b incl. the current token (0 ok)
+ *   rel_logits  fp32 [B, H_q, R]
+ *   window      > 0: sliding window of that many keys; <= 0: full causal
+ *   scale       multiplies <q, k> before the bias is added
+ *   max_seq_len host-side upper bound on seq_lens (sizes the split plan;
+ *               a longer sequence is still computed correctly)
+ *   out         bf16 [B, H_q, D], fully overwritten (never read)
+ *   lse_out     fp32 [B, H_q] natural-log lse, or NULL
+ *   workspace   device scratch of at least
+ *               inkling_rel_attn_decode_workspace_size(...) bytes when the
+ *               chosen split count is > 1; may be NULL when it is 1
+ *   num_splits  0 = automatic (inkling_rel_attn_choose_splits with the
+ *               device's SM count), > 0 = forced (clamped to [1, 128] and to
+ *               one split per 64 keys)
+ */
+int inkling_rel_attn_decode(
+    const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* page_table, int32_t page_table_stride,
+    const int32_t* seq_lens, const float* rel_logits,
+    int32_t B, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+    int32_t num_pages, int32_t R, int32_t window, float scale,
+    int32_t max_seq_len, void* out, float* lse_out, void* workspace,
+    size_t workspace_bytes, int32_t num_splits, int32_t* device_error,
+    void* stream);
+
+/*
+ * inkling_rel_attn_prefill -- chunked / paged prefill (TensorRT-LLM PR #17062,
+ * "Implementation": paged prefill over the cache).
+ *
+ * Sequence b owns the packed query tokens cu_seqlens_q[b] ..
+ * cu_seqlens_q[b+1]-1.  They are the LAST q_len_b = cu_seqlens_q[b+1] -
+ * cu_seqlens_q[b] tokens of a sequence whose seq_lens[b] keys (cached prefix
+ * plus this chunk) are all in the cache, so query i sits at position
+ * p = seq_lens[b] - q_len_b + i.
+ *
+ *   q            bf16 [T, H_q, D]
+ *   cu_seqlens_q int32 [B + 1], non-decreasing, cu_seqlens_q[0] = 0,
+ *                cu_seqlens_q[B] = T, every q_len_b <= max_q_len
+ *   seq_lens     int32 [B], q_len_b <= seq_lens[b]
+ *   rel_logits   fp32 [T, H_q, R]
+ *   max_q_len    host-side bound on q_len_b (sizes the grid)
+ *   out          bf16 [T, H_q, D]; lse_out fp32 [T, H_q] or NULL
+ *   workspace    unused by this version (pass NULL / 0)
+ * Other arguments as for decode.
+ */
+int inkling_rel_attn_prefill(
+    const void* q, const int32_t* cu_seqlens_q, const void* k_cache,
+    const void* v_cache, const int32_t* page_table, int32_t page_table_stride,
+    const int32_t* seq_lens, const float* rel_logits, int32_t B, int32_t T,
+    int32_t max_q_len, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+    int32_t num_pages, int32_t R, int32_t window, float scale,
+    int32_t max_seq_len, void* out, float* lse_out, void* workspace,
+    size_t workspace_bytes, int32_t* device_error, void* stream);
+
+/*
+ * inkling_rel_attn_choose_splits -- the decode split count, a pure host
+ * function of host scalars (so it is identical at graph capture and replay,
+ * and independent of physical page ids).  vLLM PR #51560, "Changes": the
+ * split count is computed per call and capped at 128.
+ *
+ * keys per query = min(window, max_seq_len) (or max_seq_len when window <= 0);
+ * the count aims at >= 3 CTAs per SM over B * H_kv (sequence, KV head) pairs,
+ * keeps every split >= 256 keys, caps a split at 1024 keys, and is <= 128.
+ * num_sms <= 0 means 152 (a GB300).  Returns >= 1.
+ */
+int32_t inkling_rel_attn_choose_splits(int32_t B, int32_t H_kv, int32_t window,
+                                       int32_t max_seq_len, int32_t num_sms);
+
+/*
+ * inkling_rel_attn_decode_workspace_size -- bytes of workspace decode needs
+ * for these scalars: fp32 partial outputs [B, H_q, S, D] plus fp32 partial
+ * lse [B, H_q, S], S = the split count the call will use (num_splits as for
+ * decode; 0 = automatic with num_sms SMs, num_sms <= 0 = the current device's
+ * SM count, or 152 if no device is visible).  0 when S == 1.  Host only.
+ */
+size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t H_q,
+                                              int32_t H_kv, int32_t D,
+                                              int32_t window,
+                                              int32_t max_seq_len,
+                                              int32_t num_splits,
+                                              int32_t num_sms);
+
+/* Workspace bytes prefill needs (0 in this version).  Host only. */
+size_t inkling_rel_attn_prefill_workspace_size(int32_t T, int32_t H_q,
+                                               int32_t D);
+
+/* Static, human-readable text for an INKLING_* return code. */
+const char* inkling_rel_attn_error_string(int32_t code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t inkling_rel_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INKLING_REL_ATTN_H */

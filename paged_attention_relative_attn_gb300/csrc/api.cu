@@ -1,0 +1,294 @@
+// C ABI of libinkling_rel_attn.so: argument validation, the split plan,
+// workspace sizing, device checks and error strings.  See
+// include/inkling_rel_attn.h for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+
+namespace ira {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int32_t decode_keys_max(int32_t window, int32_t max_seq_len) {
+  int32_t k = std::max<int32_t>(max_seq_len, 1);
+  if (window > 0 && window < k) k = window;
+  return k;
+}
+
+// Resolve a split request into (S, chunk): chunk is a multiple of 64 keys and
+// S = ceil(keys_max / chunk) <= 128.
+void decode_split_plan(int32_t keys_max, int32_t S_req, int32_t* S_out, int32_t* chunk_out) {
+  const int64_t keys = std::max<int32_t>(keys_max, 1);
+  int64_t S = std::max<int32_t>(S_req, 1);
+  S = std::min<int64_t>(S, 128);
+  S = std::min<int64_t>(S, ceil_div(keys, 64));
+  S = std::max<int64_t>(S, 1);
+  int64_t chunk = ceil_div(ceil_div(keys, S), 64) * 64;
+  S = ceil_div(keys, chunk);
+  if (S <= 1) {
+    S = 1;
+    chunk = std::max<int64_t>(chunk, keys);
+  }
+  *S_out = (int32_t)S;
+  *chunk_out = (int32_t)std::min<int64_t>(chunk, INT32_MAX);
+}
+
+size_t decode_workspace_bytes(int32_t B, int32_t H_q, int32_t D, int32_t S) {
+  if (S <= 1 || B <= 0 || H_q <= 0) return 0;
+  const size_t rows = (size_t)B * H_q * S;
+  return align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+// ---------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[5];
+  cuuint64_t gstride[4];
+  cuuint32_t bdim[5];
+  cuuint32_t estr[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estr[i] = 1;
+    if (i + 1 < rank) gstride[i] = strides_bytes[i];
+  }
+  CUresult r = fn(map, dtype, rank, base, gdim, gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- device info
+struct DevInfo {
+  int ok;  // 1 = sm_103, 0 = other, -1 = query failed
+  int sms;
+};
+
+static DevInfo device_info() {
+  static std::atomic<int> cached_ok[64];
+  static std::atomic<int> cached_sms[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return {-1, 0};
+  if (dev < 64) {
+    int ok = cached_ok[dev].load(std::memory_order_relaxed);
+    if (ok != 0) return {ok > 0 ? 1 : 0, cached_sms[dev].load(std::memory_order_relaxed)};
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return {-1, 0};
+  const int ok = (major == 10 && minor == 3) ? 1 : 0;
+  if (dev < 64) {
+    cached_sms[dev].store(sms, std::memory_order_relaxed);
+    cached_ok[dev].store(ok ? 1 : -1, std::memory_order_relaxed);
+  }
+  return {ok, sms};
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+static bool common_shape_ok(int32_t H_q, int32_t H_kv, int32_t D, int32_t P, int32_t num_pages,
+                            int32_t R, int32_t pt_stride) {
+  if (H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || H_q / H_kv > 16) return false;
+  if (D != 64 && D != 128) return false;
+  if (P <= 0 || P % 16 != 0 || P > 256) return false;
+  if (num_pages <= 0 || R <= 0 || pt_stride <= 0) return false;
+  if ((int64_t)pt_stride * P > INT32_MAX) return false;
+  return true;
+}
+
+}  // namespace ira
+
+using namespace ira;
+
+extern "C" {
+
+int32_t inkling_rel_attn_version(void) { return 100; }
+
+const char* inkling_rel_attn_error_string(int32_t code) {
+  switch (code) {
+    case INKLING_OK: return "success";
+    case INKLING_ERR_ARG: return "invalid argument (NULL pointer, bad scalar or unsupported shape)";
+    case INKLING_ERR_ALIGN: return "misaligned pointer (16 bytes for q/k/v/out/workspace, 4 otherwise)";
+    case INKLING_ERR_WORKSPACE: return "workspace missing or too small";
+    case INKLING_ERR_DEVICE: return "current CUDA device is not an sm_103 GPU (or no device)";
+    case INKLING_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    default: return "unknown error code";
+  }
+}
+
+int32_t inkling_rel_attn_choose_splits(int32_t B, int32_t H_kv, int32_t window, int32_t max_seq_len,
+                                       int32_t num_sms) {
+  if (num_sms <= 0) num_sms = 152;
+  const int64_t keys = decode_keys_max(window, max_seq_len);
+  if (B <= 0 || H_kv <= 0) return 1;
+  const int64_t pairs = (int64_t)B * H_kv;
+  const int64_t target = 3LL * num_sms;          // >= 3 CTAs per SM overall
+  const int64_t s_fill = (target + pairs - 1) / pairs;
+  const int64_t s_len = (keys + 255) / 256;      // each split >= 256 keys
+  const int64_t s_cap = (keys + 1023) / 1024;    // each split <= 1024 keys
+  int64_t S = std::max(s_cap, std::min(s_fill, s_len));
+  S = std::max<int64_t>(1, std::min<int64_t>(S, 128));
+  int32_t S_out, chunk;
+  decode_split_plan((int32_t)keys, (int32_t)S, &S_out, &chunk);
+  return S_out;
+}
+
+size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                                              int32_t window, int32_t max_seq_len,
+                                              int32_t num_splits, int32_t num_sms) {
+  const int32_t keys = decode_keys_max(window, max_seq_len);
+  int32_t S_req = num_splits;
+  if (S_req <= 0) {
+    if (num_sms <= 0) {
+      DevInfo di = device_info();
+      num_sms = di.ok >= 0 && di.sms > 0 ? di.sms : 152;
+    }
+    S_req = inkling_rel_attn_choose_splits(B, H_kv, window, max_seq_len, num_sms);
+  }
+  int32_t S, chunk;
+  decode_split_plan(keys, S_req, &S, &chunk);
+  return decode_workspace_bytes(B, H_q, D, S);
+}
+
+size_t inkling_rel_attn_prefill_workspace_size(int32_t T, int32_t H_q, int32_t D) {
+  (void)T;
+  (void)H_q;
+  (void)D;
+  return 0;
+}
+
+int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* page_table, int32_t page_table_stride,
+                            const int32_t* seq_lens, const float* rel_logits, int32_t B, int32_t H_q,
+                            int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, int32_t R,
+                            int32_t window, float scale, int32_t max_seq_len, void* out,
+                            float* lse_out, void* workspace, size_t workspace_bytes,
+                            int32_t num_splits, int32_t* device_error, void* stream) {
+  if (B < 0 || max_seq_len < 0) return INKLING_ERR_ARG;
+  if (!common_shape_ok(H_q, H_kv, D, page_size, num_pages, R, page_table_stride)) return INKLING_ERR_ARG;
+  if (!(scale == scale)) return INKLING_ERR_ARG;
+  if (B == 0) return INKLING_OK;
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !rel_logits || !out)
+    return INKLING_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(rel_logits, 4) ||
+      !aligned(lse_out, 4) || !aligned(device_error, 4) || !aligned(workspace, 16))
+    return INKLING_ERR_ALIGN;
+  const DevInfo di = device_info();
+  if (di.ok != 1) return INKLING_ERR_DEVICE;
+
+  DecodeCall c;
+  c.q = q;
+  c.k_cache = k_cache;
+  c.v_cache = v_cache;
+  c.page_table = page_table;
+  c.pt_stride = page_table_stride;
+  c.seq_lens = seq_lens;
+  c.rel = rel_logits;
+  c.B = B;
+  c.H_q = H_q;
+  c.H_kv = H_kv;
+  c.D = D;
+  c.P = page_size;
+  c.num_pages = num_pages;
+  c.R = R;
+  c.window = window;
+  c.scale = scale;
+  c.keys_max = decode_keys_max(window, max_seq_len);
+  const int32_t S_req =
+      num_splits > 0 ? num_splits : inkling_rel_attn_choose_splits(B, H_kv, window, max_seq_len, di.sms);
+  decode_split_plan(c.keys_max, S_req, &c.S, &c.chunk);
+  c.out = out;
+  c.lse_out = lse_out;
+  c.o_part = nullptr;
+  c.lse_part = nullptr;
+  if (c.S > 1) {
+    const size_t need = decode_workspace_bytes(B, H_q, D, c.S);
+    if (!workspace || workspace_bytes < need) return INKLING_ERR_WORKSPACE;
+    const size_t rows = (size_t)B * H_q * c.S;
+    c.o_part = static_cast<float*>(workspace);
+    c.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * D * sizeof(float)));
+  }
+  c.dev_err = device_error;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return launch_decode(c);
+}
+
+int inkling_rel_attn_prefill(const void* q, const int32_t* cu_seqlens_q, const void* k_cache,
+                             const void* v_cache, const int32_t* page_table, int32_t page_table_stride,
+                             const int32_t* seq_lens, const float* rel_logits, int32_t B, int32_t T,
+                             int32_t max_q_len, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+                             int32_t num_pages, int32_t R, int32_t window, float scale,
+                             int32_t max_seq_len, void* out, float* lse_out, void* workspace,
+                             size_t workspace_bytes, int32_t* device_error, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (B < 0 || T < 0 || max_q_len < 0 || max_seq_len < 0) return INKLING_ERR_ARG;
+  if (!common_shape_ok(H_q, H_kv, D, page_size, num_pages, R, page_table_stride)) return INKLING_ERR_ARG;
+  if (R % 4 != 0) return INKLING_ERR_ARG;
+  if (!(scale == scale)) return INKLING_ERR_ARG;
+  if (B == 0 || T == 0) return INKLING_OK;
+  if (!q || !cu_seqlens_q || !k_cache || !v_cache || !page_table || !seq_lens || !rel_logits || !out)
+    return INKLING_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(rel_logits, 16) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(lse_out, 4) || !aligned(device_error, 4))
+    return INKLING_ERR_ALIGN;
+  const DevInfo di = device_info();
+  if (di.ok != 1) return INKLING_ERR_DEVICE;
+  PrefillCall c;
+  c.q = q;
+  c.cu_seqlens_q = cu_seqlens_q;
+  c.k_cache = k_cache;
+  c.v_cache = v_cache;
+  c.page_table = page_table;
+  c.pt_stride = page_table_stride;
+  c.seq_lens = seq_lens;
+  c.rel = rel_logits;
+  c.B = B;
+  c.T = T;
+  c.max_q_len = max_q_len;
+  c.H_q = H_q;
+  c.H_kv = H_kv;
+  c.D = D;
+  c.P = page_size;
+  c.num_pages = num_pages;
+  c.R = R;
+  c.window = window;
+  c.scale = scale;
+  c.max_seq_len = max_seq_len;
+  c.out = out;
+  c.lse_out = lse_out;
+  c.dev_err = device_error;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return launch_prefill(c);
+}
+
+}  // extern "C"

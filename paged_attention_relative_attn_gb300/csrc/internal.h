@@ -1,0 +1,67 @@
+// Host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/inkling_rel_attn.h"
+
+namespace ira {
+
+// Validated decode call, with the split plan resolved.
+struct DecodeCall {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* page_table;
+  int32_t pt_stride;
+  const int32_t* seq_lens;
+  const float* rel;
+  int32_t B, H_q, H_kv, D, P, num_pages, R, window;
+  float scale;
+  int32_t keys_max;  // host bound on visible keys per query
+  int32_t S;         // split count (grid.x)
+  int32_t chunk;     // keys per split (multiple of 64)
+  void* out;
+  float* lse_out;
+  float* o_part;     // [B, H_q, S, D] when S > 1
+  float* lse_part;   // [B, H_q, S]   when S > 1
+  int32_t* dev_err;
+  cudaStream_t stream;
+};
+
+struct PrefillCall {
+  const void* q;
+  const int32_t* cu_seqlens_q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* page_table;
+  int32_t pt_stride;
+  const int32_t* seq_lens;
+  const float* rel;
+  int32_t B, T, max_q_len, H_q, H_kv, D, P, num_pages, R, window;
+  float scale;
+  int32_t max_seq_len;
+  void* out;
+  float* lse_out;
+  int32_t* dev_err;
+  cudaStream_t stream;
+};
+
+int launch_decode(const DecodeCall& c);    // returns INKLING_* code
+int launch_prefill(const PrefillCall& c);  // returns INKLING_* code
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle);
+
+// Split plan shared by the ABI helpers and the launcher.
+int32_t decode_keys_max(int32_t window, int32_t max_seq_len);
+void decode_split_plan(int32_t keys_max, int32_t S_req, int32_t* S_out, int32_t* chunk_out);
+size_t decode_workspace_bytes(int32_t B, int32_t H_q, int32_t D, int32_t S);
+size_t align256(size_t x);
+
+}  // namespace ira
