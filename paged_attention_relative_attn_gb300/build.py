@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libinkling_rel_attn.so")
 SOURCES = ["api.cu", "decode.cu", "prefill.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "tc.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "tc.cuh", "plan.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",

@@ -42,10 +42,12 @@ void decode_split_plan(int32_t keys_max, int32_t S_req, int32_t* S_out, int32_t*
   *chunk_out = (int32_t)std::min<int64_t>(chunk, INT32_MAX);
 }
 
+// Workspace layout when S > 1: [work-item counter, 256 B][o_part fp32
+// B*H_q*S*D][lse_part fp32 B*H_q*S], each part 256-byte aligned.
 size_t decode_workspace_bytes(int32_t B, int32_t H_q, int32_t D, int32_t S) {
   if (S <= 1 || B <= 0 || H_q <= 0) return 0;
   const size_t rows = (size_t)B * H_q * S;
-  return align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
+  return 256 + align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -229,12 +231,15 @@ int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_ca
   c.lse_out = lse_out;
   c.o_part = nullptr;
   c.lse_part = nullptr;
+  c.counter = nullptr;
   if (c.S > 1) {
     const size_t need = decode_workspace_bytes(B, H_q, D, c.S);
     if (!workspace || workspace_bytes < need) return INKLING_ERR_WORKSPACE;
     const size_t rows = (size_t)B * H_q * c.S;
-    c.o_part = static_cast<float*>(workspace);
-    c.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * D * sizeof(float)));
+    char* ws = static_cast<char*>(workspace);
+    c.counter = reinterpret_cast<int32_t*>(ws);
+    c.o_part = reinterpret_cast<float*>(ws + 256);
+    c.lse_part = reinterpret_cast<float*>(ws + 256 + align256(rows * D * sizeof(float)));
   }
   c.dev_err = device_error;
   c.stream = static_cast<cudaStream_t>(stream);

@@ -6,27 +6,32 @@
 // "Implementation"; split-KV from Fail fast on Inkling's unsupported GPU
 // architectures, vLLM PR #51560, "Changes").
 //
-// Design (one CTA per (split, KV head, sequence)):
-//  * warp 4 (producer) walks the CTA's logical key range in tiles of <= 64
-//    keys, looks the physical page up in the page table and issues TMA loads
-//    of the K and V rows of this KV head (box = 64 dims x 1 head x rows x 1
-//    page, 128-byte swizzle) into a ring of shared-memory stages guarded by
-//    full/empty mbarriers.  The first tile of a range starts mid-page so the
-//    box runs past the page end (zero-filled, never read from HBM); the last
-//    tile is placed so the box starts before the page (also zero-filled).
-//    Only the bytes of visible keys are fetched.
-//  * warps 0-3 (consumers) each own 16 rows of every tile and compute the
-//    transposed products S^T = K Q^T and O^T += V^T P^T with mma.sync
-//    m16n8k16 (the GQA group of <= 8 query heads is the N=8 side, so no
-//    padding of M), add the bias from a shared-memory copy of the needed
-//    slice of rel_logits (pre-multiplied by log2 e), mask, and run an online
-//    softmax per head with warp shuffles over the keys.  P is moved from the
-//    accumulator layout into the B-operand layout with movmatrix.
-//  * at the end the four warps' (m, l, O) are combined through shared memory
-//    and written either as the final bf16 output or, when the sequence spans
-//    several splits, as a normalised fp32 partial plus its lse for the merge.
-// Reduction order depends only on logical key positions and host scalars, so
-// results are bit-identical under any physical page permutation.
+// Design: a persistent grid (two CTAs per SM) walks work items
+// (sequence, KV head, split).  Each CTA has
+//  * a producer warp (warp 4) that takes the next item (static stride, or an
+//    atomic counter when splits make items uneven), publishes the item's key
+//    range to the consumers through a small shared-memory ring, and walks the
+//    range in tiles of <= 64 keys: it looks the physical page up in the page
+//    table and issues TMA loads of that KV head's K and V rows (box = 64 dims x
+//    1 head x rows x 1 page, 128-byte swizzle) into a ring of stages guarded by
+//    full/empty mbarriers.  The first tile of a range starts mid-page so its
+//    box runs past the page end (zero-filled, never fetched); the last tile is
+//    placed so its box starts before the page (also zero-filled): only the
+//    bytes of visible keys are read.  The ring runs across item boundaries, so
+//    the next item's K/V stream in while the consumers finish the current one.
+//  * four consumer warps that each own 16 rows of every tile and compute the
+//    transposed products S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16
+//    (the GQA group of <= 8 query heads is the N = 8 side, so M is never
+//    padded), add the bias from a shared-memory copy of the needed slice of
+//    rel_logits (pre-multiplied by log2 e), mask, and keep an online softmax
+//    per head with warp shuffles over the keys.  P goes from the accumulator
+//    layout to the B-operand layout with movmatrix.  At the end of an item the
+//    four warps' (m, l, O) are combined through shared memory and written as
+//    the final bf16 output or, when the sequence spans several splits, as a
+//    normalised fp32 partial plus its lse for the merge kernel.
+// Reduction order depends only on logical key positions and host scalars,
+// never on page ids or on which CTA ran an item, so results are bit-identical
+// under any physical page permutation and any schedule.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -35,14 +40,28 @@
 #include <mutex>
 
 #include "internal.h"
+#include "plan.cuh"
 #include "ptx.cuh"
 
 namespace ira {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
-constexpr int kTileRows = 64;
-constexpr int kHalfBytes = kTileRows * 128;  // 64 rows x 64 bf16
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kDecodeThreads = kConsumerThreads + 32;
+constexpr int kItemSlots = 4;
+#ifndef INKLING_DECODE_CTAS_PER_SM
+#define INKLING_DECODE_CTAS_PER_SM 2
+#endif
+#ifndef INKLING_DECODE_SMEM_BUDGET_KB
+#define INKLING_DECODE_SMEM_BUDGET_KB 110
+#endif
+#ifndef INKLING_DECODE_MAX_STAGES
+#define INKLING_DECODE_MAX_STAGES 4
+#endif
+#ifndef INKLING_DECODE_BALANCED
+#define INKLING_DECODE_BALANCED 1
+#endif
+constexpr int kCtasPerSm = INKLING_DECODE_CTAS_PER_SM;
 
 struct DecodeParams {
   CUtensorMap tmap_k;  // [num_pages][P][H_kv][D] bf16, box {64, 1, BH, 1}
@@ -56,8 +75,10 @@ struct DecodeParams {
   float* o_part;
   float* lse_part;
   int32_t* dev_err;
-  int pt_stride, H_q, H_kv, G, P, num_pages, R, window;
+  int32_t* counter;  // dynamic scheduling (zeroed before launch), or nullptr
+  int B, pt_stride, H_q, H_kv, G, P, num_pages, R, window;
   int S, chunk, stages, nb;
+  int total_items;
   float scale_log2;
 };
 
@@ -81,76 +102,34 @@ __device__ __forceinline__ SeqPlan seq_plan(int L, int pt_stride, int P, int win
   return s;
 }
 
-// One tile of the logical key range: rows r of the stage hold key jbase + r;
-// keys [klo, khi] are the valid ones.
-struct Tile {
-  int jbase, klo, khi;
+// One work item as published by the producer: keys [a, e] of sequence b,
+// KV head hkv, split `split` of n_s; the decode query sits at pos.
+struct ItemRec {
+  int b, hkv, split, n_s, a, e, pos, nvis;
 };
 
-// Tile walk for page sizes that are a multiple of 64 (box of 64 rows): tiles
-// never cross a page; see the file comment for the placement of the first
-// and last tile.
-struct PlanBig {
-  int e, P, jt;
-  __device__ PlanBig(int a, int e_, int P_) : e(e_), P(P_), jt(a) {}
-  __device__ bool done() const { return jt > e; }
-  // returns the tile and, for the loader, the logical page and first slot
-  __device__ Tile next(int& lpage, int& slot0) {
-    const int lp = jt / P;
-    const int pstart = lp * P;
-    const int pe = pstart + P - 1;
-    int et = min(jt + 63, pe);
-    et = min(et, e);
-    const bool rev = (et == e) && (jt == pstart) && (et - jt < 63);
-    Tile t;
-    t.jbase = rev ? et - 63 : jt;
-    t.klo = jt;
-    t.khi = et;
-    lpage = lp;
-    slot0 = t.jbase - pstart;
-    jt = et + 1;
-    return t;
+// Shared-memory layout (byte offsets from the 1024-aligned base), computed
+// identically on host and device.
+struct DecodeSmem {
+  int stage_bytes, stages, bias_off, comb_off, ring_off, bar_off, total;
+  __host__ __device__ DecodeSmem(int D, int G, int NT, int nb, int stages_) {
+    stage_bytes = 2 * (D / 64) * kHalfBytes;
+    stages = stages_;
+    bias_off = stages * stage_bytes;
+    const int bias_bytes = ((G * nb * 4 + 127) / 128) * 128;
+    comb_off = bias_off + bias_bytes;
+    const int comb_bytes = kConsumerWarps * G * (D + 4) * 4 + 2 * kConsumerWarps * 8 * NT * 4;
+    ring_off = comb_off + ((comb_bytes + 127) / 128) * 128;
+    bar_off = ring_off + kItemSlots * (int)sizeof(ItemRec);
+    total = bar_off + (2 * stages + 2 * kItemSlots) * 8 + 16;
   }
 };
-
-// Tile walk for other page sizes (multiple of 16): 64-aligned logical
-// blocks, each assembled from four 16-row boxes; boxes that hold no valid key
-// are not loaded.
-struct PlanSmall {
-  int a, e, jt;
-  __device__ PlanSmall(int a_, int e_) : a(a_), e(e_), jt(a_ & ~63) {}
-  __device__ bool done() const { return jt > e; }
-  __device__ Tile next() {
-    Tile t;
-    t.jbase = jt;
-    t.klo = max(a, jt);
-    t.khi = min(e, jt + 63);
-    jt += 64;
-    return t;
-  }
-};
-
-template <int BH>
-struct PlanSel;
-template <>
-struct PlanSel<64> {
-  using type = PlanBig;
-};
-template <>
-struct PlanSel<16> {
-  using type = PlanSmall;
-};
-
-__device__ __forceinline__ void report(int32_t* err, int bit) {
-  if (err) atomicOr(err, bit);
-}
 
 template <int D, int NT, int BH>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int HALVES = D / 64;
   constexpr int TILE_BYTES = HALVES * kHalfBytes;
-  constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int HP = 8 * NT;  // padded heads per group
 
@@ -158,53 +137,39 @@ __global__ void __launch_bounds__(kDecodeThreads)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int split = blockIdx.x;
-  const int hkv = blockIdx.y;
-  const int b = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int G = p.G;
   const int S = p.S;
+  const DecodeSmem L(D, G, NT, p.nb, p.stages);
+  const int stages = L.stages;
+  const int STAGE_BYTES = L.stage_bytes;
 
-  const int Lraw = p.seq_lens[b];
-  const SeqPlan sp = seq_plan(Lraw, p.pt_stride, p.P, p.window, p.chunk, S);
-  if (Lraw > p.pt_stride * p.P && tid == 0 && split == 0 && hkv == 0)
-    report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
-  if (split >= max(sp.n_s, 1)) return;
-  const bool final_out = sp.n_s <= 1;
-
-  if (sp.nvis == 0) {  // empty sequence: out = 0, lse = -inf
-    for (int i = tid; i < G * D; i += kDecodeThreads) {
-      const int h = i / D, d = i - h * D;
-      const size_t row = (size_t)b * p.H_q + hkv * G + h;
-      p.out[row * D + d] = __float2bfloat16(0.f);
-      if (d == 0 && p.lse_out) p.lse_out[row] = -INFINITY;
-    }
-    return;
-  }
-
-  const int a = sp.lo + split * p.chunk;
-  const int e = (split == sp.n_s - 1) ? sp.pos : a + p.chunk - 1;
-
-  // ---- shared memory carve-up
-  const int stages = p.stages;
-  float* bias_s = reinterpret_cast<float*>(smem + stages * STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * STAGE_BYTES + ((G * p.nb * 4 + 15) & ~15));
-  // full[s] = bars[s], empty[s] = bars[stages + s]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * stages);
+  float* bias_s = reinterpret_cast<float*>(smem + L.bias_off);
+  float* comb_o = reinterpret_cast<float*>(smem + L.comb_off);  // [4][G][D+4]
+  float* comb_m = comb_o + kConsumerWarps * G * (D + 4);          // [4][HP]
+  float* comb_l = comb_m + kConsumerWarps * HP;                   // [4][HP]
+  ItemRec* ring = reinterpret_cast<ItemRec*>(smem + L.ring_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  // full[s] = bars[s], empty[s] = bars[stages+s]; item ring barriers after
+  uint64_t* ifull = bars + 2 * stages;
+  uint64_t* iempty = ifull + kItemSlots;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(iempty + kItemSlots);
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
       mbar_init(smem_u32(&bars[stages + s]), kConsumerWarps);
     }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(smem_u32(&ifull[i]), 1);
+      mbar_init(smem_u32(&iempty[i]), kConsumerWarps);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
-
-  using Plan = typename PlanSel<BH>::type;
 
   // =================================================================== producer
   if (warp == kConsumerWarps) {
@@ -213,85 +178,139 @@ __global__ void __launch_bounds__(kDecodeThreads)
       tmap_prefetch(&p.tmap_v);
     }
     const uint64_t pol = policy_evict_first();
-    const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride;
-    int batch_base = -1000000;
-    int my_page = 0;
-    auto page_of = [&](int lp) -> int {  // warp-uniform
-      if (lp < batch_base || lp >= batch_base + 32) {
-        batch_base = lp;
-        const int idx = lp + lane;
-        my_page = (idx < p.pt_stride) ? __ldg(pt_row + idx) : 0;
-      }
-      return __shfl_sync(0xffffffffu, my_page, lp - batch_base);
-    };
-    Plan plan = [&]() {
-      if constexpr (BH == 64) return PlanBig(a, e, p.P);
-      else return PlanSmall(a, e);
-    }();
-    int k = 0;
+    int kt = 0;  // tiles issued (global over items)
+    int ki = 0;  // items published
     bool ok = true;
-    while (!plan.done()) {
-      const int st = k % stages;
-      if (k >= stages && lane == 0) ok = mbar_wait(smem_u32(&bars[stages + st]), ((k / stages) - 1) & 1, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const uint32_t kdst = smem_u32(smem + st * STAGE_BYTES);
-      const uint32_t vdst = kdst + TILE_BYTES;
-      const uint32_t fb = smem_u32(&bars[st]);
-      if constexpr (BH == 64) {
-        int lp, slot0;
-        plan.next(lp, slot0);
-        int page = page_of(lp);
-        if (page < 0 || page >= p.num_pages) {
-          if (lane == 0) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
-        }
+    for (int n = 0;; ++n) {
+      int id = 0;
+      if (p.counter) {
+        if (lane == 0) id = atomicAdd(p.counter, 1);
+        id = __shfl_sync(0xffffffffu, id, 0);
+      } else {
+        id = blockIdx.x + n * gridDim.x;
+      }
+      ItemRec r;
+      r.b = -1;
+      r.hkv = r.split = r.n_s = r.a = r.e = r.pos = r.nvis = 0;
+      if (id < p.total_items) {
+        r.split = id % S;
+        const int rest = id / S;
+        r.hkv = rest % p.H_kv;
+        r.b = rest / p.H_kv;
+        const int Lraw = __ldg(p.seq_lens + r.b);
+        const SeqPlan sp = seq_plan(Lraw, p.pt_stride, p.P, p.window, p.chunk, S);
+        if (r.split >= max(sp.n_s, 1)) continue;  // empty split: nothing to do
+        if (Lraw > p.pt_stride * p.P && lane == 0 && r.hkv == 0 && r.split == 0)
+          report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
+        r.n_s = sp.n_s;
+        r.pos = sp.pos;
+        r.nvis = sp.nvis;
+        r.a = sp.lo + r.split * p.chunk;
+        r.e = (r.split == sp.n_s - 1) ? sp.pos : r.a + p.chunk - 1;
+      }
+      // publish the item
+      {
+        const int slot = ki % kItemSlots;
+        if (ki >= kItemSlots && lane == 0)
+          ok = mbar_wait(smem_u32(&iempty[slot]), ((ki / kItemSlots) - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
+          ring[slot] = r;
+          mbar_arrive(smem_u32(&ifull[slot]));
+        }
+        ++ki;
+      }
+      if (r.b < 0) break;
+      if (r.nvis == 0) continue;
+
+      const int32_t* pt_row = p.page_table + (size_t)r.b * p.pt_stride;
+      int batch_base = -1000000;
+      int my_page = 0;
+      auto page_of = [&](int lp) -> int {  // warp-uniform
+        if (lp < batch_base || lp >= batch_base + 32) {
+          batch_base = lp;
+          const int idx = lp + lane;
+          my_page = (idx < p.pt_stride) ? __ldg(pt_row + idx) : 0;
+        }
+        return __shfl_sync(0xffffffffu, my_page, lp - batch_base);
+      };
+
+      if constexpr (BH == 64) {
+        PlanBig plan(r.a, r.e, p.P);
+        while (!plan.done()) {
+          const int st = kt % stages;
+          if (kt >= stages && lane == 0)
+            ok = mbar_wait(smem_u32(&bars[stages + st]), ((kt / stages) - 1) & 1, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          int lp, slot0;
+          plan.next(lp, slot0);
+          const int page = page_of(lp);
+          if (lane == 0) {
+            if (page < 0 || page >= p.num_pages) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+            const uint32_t kdst = smem_u32(smem + st * STAGE_BYTES);
+            const uint32_t vdst = kdst + TILE_BYTES;
+            const uint32_t fb = smem_u32(&bars[st]);
+            mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
 #pragma unroll
-          for (int h = 0; h < HALVES; ++h) {
-            tma_load_4d(kdst + h * kHalfBytes, &p.tmap_k, fb, h * 64, hkv, slot0, page, pol);
-            tma_load_4d(vdst + h * kHalfBytes, &p.tmap_v, fb, h * 64, hkv, slot0, page, pol);
+            for (int h = 0; h < HALVES; ++h) {
+              tma_load_4d(kdst + h * kHalfBytes, &p.tmap_k, fb, h * 64, r.hkv, slot0, page, pol);
+              tma_load_4d(vdst + h * kHalfBytes, &p.tmap_v, fb, h * 64, r.hkv, slot0, page, pol);
+            }
           }
+          __syncwarp();
+          ++kt;
         }
       } else {
-        const Tile t = plan.next();
-        int nbox = 0;
-        int pages[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int k0 = t.jbase + 16 * c;
-          const bool need = (k0 <= t.khi) && (k0 + 15 >= t.klo);
-          pages[c] = need ? page_of(k0 / p.P) : 0;
-          if (need) {
-            ++nbox;
-            if ((pages[c] < 0 || pages[c] >= p.num_pages) && lane == 0)
-              report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
-          }
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, nbox * 2 * HALVES * 16 * 128);
+        PlanSmall plan(r.a, r.e);
+        while (!plan.done()) {
+          const int st = kt % stages;
+          if (kt >= stages && lane == 0)
+            ok = mbar_wait(smem_u32(&bars[stages + st]), ((kt / stages) - 1) & 1, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          const Tile t = plan.next();
+          int nbox = 0;
+          int pages[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int k0 = t.jbase + 16 * c;
-            if (!((k0 <= t.khi) && (k0 + 15 >= t.klo))) continue;
-            const int slot = k0 % p.P;
+            const bool need = (k0 <= t.khi) && (k0 + 15 >= t.klo);
+            pages[c] = need ? page_of(k0 / p.P) : 0;
+            nbox += need ? 1 : 0;
+          }
+          if (lane == 0) {
+            const uint32_t kdst = smem_u32(smem + st * STAGE_BYTES);
+            const uint32_t vdst = kdst + TILE_BYTES;
+            const uint32_t fb = smem_u32(&bars[st]);
+            mbar_arrive_expect_tx(fb, nbox * 2 * HALVES * 16 * 128);
 #pragma unroll
-            for (int h = 0; h < HALVES; ++h) {
-              tma_load_4d(kdst + h * kHalfBytes + c * 16 * 128, &p.tmap_k, fb, h * 64, hkv, slot,
-                          pages[c], pol);
-              tma_load_4d(vdst + h * kHalfBytes + c * 16 * 128, &p.tmap_v, fb, h * 64, hkv, slot,
-                          pages[c], pol);
+            for (int c = 0; c < 4; ++c) {
+              const int k0 = t.jbase + 16 * c;
+              if (!((k0 <= t.khi) && (k0 + 15 >= t.klo))) continue;
+              if (pages[c] < 0 || pages[c] >= p.num_pages)
+                report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+              const int slot = k0 % p.P;
+#pragma unroll
+              for (int h = 0; h < HALVES; ++h) {
+                tma_load_4d(kdst + h * kHalfBytes + c * 16 * 128, &p.tmap_k, fb, h * 64, r.hkv,
+                            slot, pages[c], pol);
+                tma_load_4d(vdst + h * kHalfBytes + c * 16 * 128, &p.tmap_v, fb, h * 64, r.hkv,
+                            slot, pages[c], pol);
+              }
             }
           }
+          __syncwarp();
+          ++kt;
         }
       }
-      __syncwarp();
-      ++k;
+      if (!ok) break;
     }
     if (!ok && lane == 0) {
       report(p.dev_err, INKLING_DEVERR_TIMEOUT);
       // drain: wait for the copies already issued into stages nobody consumes
-      for (int j = max(0, k - stages); j < k; ++j)
+      for (int j = max(0, kt - stages); j < kt; ++j)
         mbar_wait_drain(smem_u32(&bars[j % stages]), (j / stages) & 1);
     }
     return;
@@ -300,49 +319,6 @@ __global__ void __launch_bounds__(kDecodeThreads)
   // =================================================================== consumers
   const int g = lane >> 2;  // accumulator row group
   const int c4 = lane & 3;  // thread in group
-
-  // Q^T fragments (B operand): head g (+8 per n-tile), dims 16ks + 2c4 (+8)
-  uint32_t qf[KS][NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int head = nt * 8 + g;
-    const bool live = head < G;
-    const __nv_bfloat16* qrow = p.q + ((size_t)b * p.H_q + hkv * G + (live ? head : 0)) * D;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qf[ks][nt][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4)) : 0u;
-      qf[ks][nt][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8)) : 0u;
-    }
-  }
-
-  // bias slice: distances [dlo, dhi] (clamped to R-1) for the G heads
-  const int R = p.R;
-  const int dlo = min(sp.pos - e, R - 1);
-  const int dhi = min(sp.pos - a, R - 1);
-  const int cnt = dhi - dlo + 1;
-  const bool bias_in_smem = cnt <= p.nb;
-  const float* rel_g = p.rel + ((size_t)b * p.H_q + hkv * G) * R;
-  if (bias_in_smem) {
-    for (int i = tid; i < G * cnt; i += 32 * kConsumerWarps) {
-      const int h = i / cnt, kk = i - h * cnt;
-      bias_s[h * p.nb + kk] = __ldg(rel_g + (size_t)h * R + dlo + kk) * kLog2e;
-    }
-  }
-  named_bar_sync(1, 32 * kConsumerWarps);
-
-  float m_run[NT][2], l_run[NT][2];
-  float o_acc[KS][NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o_acc[mt][nt][i] = 0.f;
-  }
-
-  // per-thread ldmatrix addressing inside a stage
   const int r0 = warp * 16;
   const int k_row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;  // K: matrices (rows, chunk)
   const int k_chi = lane >> 4;
@@ -350,31 +326,79 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const int v_chi = (lane >> 3) & 1;
   const int sw = lane & 7;  // (row & 7) for the 128-byte swizzle
   const float sl2 = p.scale_log2;
+  const int R = p.R;
 
-  Plan plan = [&]() {
-    if constexpr (BH == 64) return PlanBig(a, e, p.P);
-    else return PlanSmall(a, e);
-  }();
-  int k = 0;
+  int kt = 0;
   bool ok = true;
-  while (!plan.done()) {
-    Tile t;
-    if constexpr (BH == 64) {
-      int lp, s0;
-      t = plan.next(lp, s0);
-    } else {
-      t = plan.next();
-    }
-    const int st = k % stages;
-    bool got = true;
-    if (lane == 0) got = mbar_wait(smem_u32(&bars[st]), (k / stages) & 1, abort_flag);
-    got = __shfl_sync(0xffffffffu, got, 0);
+  for (int ki = 0;; ++ki) {
+    // ---- next item
+    const int slot = ki % kItemSlots;
+    const bool got = mbar_wait_warp(smem_u32(&ifull[slot]), (ki / kItemSlots) & 1, abort_flag);
     if (!got) {
       ok = false;
       break;
     }
-    const int key0 = t.jbase + r0;  // key of this warp's first row
-    if (key0 <= t.khi && key0 + 15 >= t.klo) {
+    const ItemRec r = ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&iempty[slot]));
+    if (r.b < 0) break;
+    const bool final_out = r.n_s <= 1;
+
+    if (r.nvis == 0) {  // empty sequence: out = 0, lse = -inf
+      for (int i = tid; i < G * D; i += kConsumerThreads) {
+        const int h = i / D, d = i - h * D;
+        const size_t row = (size_t)r.b * p.H_q + r.hkv * G + h;
+        p.out[row * D + d] = __float2bfloat16(0.f);
+        if (d == 0 && p.lse_out) p.lse_out[row] = -INFINITY;
+      }
+      continue;
+    }
+
+    // ---- per-item prologue: Q^T fragments and the bias slice
+    uint32_t qf[KS][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int head = nt * 8 + g;
+      const bool live = head < G;
+      const __nv_bfloat16* qrow =
+          p.q + ((size_t)r.b * p.H_q + r.hkv * G + (live ? head : 0)) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf[ks][nt][0] =
+            live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4)) : 0u;
+        qf[ks][nt][1] =
+            live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8)) : 0u;
+      }
+    }
+    const int dlo = min(r.pos - r.e, R - 1);
+    const int dhi = min(r.pos - r.a, R - 1);
+    const int cnt = dhi - dlo + 1;
+    const bool bias_in_smem = cnt <= p.nb;
+    const float* rel_g = p.rel + ((size_t)r.b * p.H_q + r.hkv * G) * R;
+    named_bar_sync(1, kConsumerThreads);  // previous item's readers of bias_s / comb are done
+    if (bias_in_smem) {
+      for (int i = tid; i < G * cnt; i += kConsumerThreads) {
+        const int h = i / cnt, kk = i - h * cnt;
+        bias_s[h * p.nb + kk] = __ldg(rel_g + (size_t)h * R + dlo + kk) * kLog2e;
+      }
+    }
+    named_bar_sync(1, kConsumerThreads);
+
+    float m_run[NT][2], l_run[NT][2];
+    float o_acc[KS][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o_acc[mt][nt][i] = 0.f;
+    }
+
+    auto tile_body = [&](const Tile& t, int st) {
+      const int key0 = t.jbase + r0;  // key of this warp's first row
+      if (!(key0 <= t.khi && key0 + 15 >= t.klo)) return;
       const bool part = (key0 < t.klo) || (key0 + 15 > t.khi);
       const uint32_t kb = smem_u32(smem + st * STAGE_BYTES);
       const uint32_t vb = kb + TILE_BYTES;
@@ -388,11 +412,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int chunk = 2 * ks + k_chi;
-        const uint32_t addr = kb + (chunk >> 3) * kHalfBytes + k_row * 128 + (((chunk & 7) ^ sw) << 4);
+        const uint32_t addr =
+            kb + (chunk >> 3) * kHalfBytes + k_row * 128 + (((chunk & 7) ^ sw) << 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
       }
 
       // ---- scale + bias + mask (log2 domain)
@@ -408,12 +434,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
           const int kr = i >> 1;
           int h = nt * 8 + 2 * c4 + (i & 1);
           h = h < G ? h : G - 1;
-          const int dist = sp.pos - (key0 + g + 8 * kr);
-          const int dcl = min(dist, R - 1);
+          const int dcl = min(r.pos - (key0 + g + 8 * kr), R - 1);
           float bias;
           if (bias_in_smem) {
-            const int di = vk[kr] ? dcl - dlo : 0;
-            bias = bias_s[h * p.nb + di];
+            bias = bias_s[h * p.nb + (vk[kr] ? dcl - dlo : 0)];
           } else {
             bias = vk[kr] ? __ldg(rel_g + (size_t)h * R + dcl) * kLog2e : 0.f;
           }
@@ -470,7 +494,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         const int chunk = 2 * mt + v_chi;
-        const uint32_t addr = vb + (chunk >> 3) * kHalfBytes + v_row * 128 + (((chunk & 7) ^ sw) << 4);
+        const uint32_t addr =
+            vb + (chunk >> 3) * kHalfBytes + v_row * 128 + (((chunk & 7) ^ sw) << 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(addr, a0, a1, a2, a3);
         a0 &= zm01;
@@ -478,80 +503,103 @@ __global__ void __launch_bounds__(kDecodeThreads)
         a2 &= zm89;
         a3 &= zm89;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(o_acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816(o_acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+      }
+    };
+
+    // ---- tile loop (same walk as the producer)
+    auto consume = [&](const Tile& t) -> bool {
+      const int st = kt % stages;
+      if (!mbar_wait_warp(smem_u32(&bars[st]), (kt / stages) & 1, abort_flag)) return false;
+      tile_body(t, st);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[stages + st]));
+      ++kt;
+      return true;
+    };
+    if constexpr (BH == 64) {
+      PlanBig plan(r.a, r.e, p.P);
+      while (!plan.done()) {
+        int lp, s0;
+        const Tile t = plan.next(lp, s0);
+        if (!consume(t)) {
+          ok = false;
+          break;
+        }
+      }
+    } else {
+      PlanSmall plan(r.a, r.e);
+      while (!plan.done()) {
+        if (!consume(plan.next())) {
+          ok = false;
+          break;
+        }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&bars[stages + st]));
-    ++k;
-  }
+    if (!ok) break;
 
-  // ---- finish: sum l over the 16 keys' lanes
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float v = l_run[nt][j];
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      l_run[nt][j] = v;
-    }
-
-  named_bar_sync(1, 32 * kConsumerWarps);  // all stages consumed; reuse them
-  if (!ok || *abort_flag) {
-    if (tid == 0) report(p.dev_err, INKLING_DEVERR_TIMEOUT);
-    return;
-  }
-  constexpr int OP = D + 4;  // padded row of the combine buffer
-  float* comb_o = reinterpret_cast<float*>(smem);                  // [4][HP][OP]
-  float* comb_m = comb_o + kConsumerWarps * HP * OP;               // [4][HP]
-  float* comb_l = comb_m + kConsumerWarps * HP;                    // [4][HP]
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int dim = 16 * mt + g + 8 * (i >> 1);
-        const int head = nt * 8 + 2 * c4 + (i & 1);
-        comb_o[(warp * HP + head) * OP + dim] = o_acc[mt][nt][i];
-      }
-  if (g == 0) {
+    // ---- finish the item: sum l over the lanes of the 16 keys
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int head = nt * 8 + 2 * c4 + j;
-        comb_m[warp * HP + head] = m_run[nt][j];
-        comb_l[warp * HP + head] = l_run[nt][j];
+        float v = l_run[nt][j];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        l_run[nt][j] = v;
       }
-  }
-  named_bar_sync(1, 32 * kConsumerWarps);
-
-  for (int i = tid; i < G * D; i += 32 * kConsumerWarps) {
-    const int h = i / D, d = i - h * D;
-    float M = -INFINITY;
+    constexpr int OP = D + 4;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * HP + h]);
-    float Ls = 0.f, o = 0.f;
+    for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float sc = ex2(comb_m[w * HP + h] - M);
-      Ls = fmaf(sc, comb_l[w * HP + h], Ls);
-      o = fmaf(sc, comb_o[(w * HP + h) * OP + d], o);
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int head = nt * 8 + 2 * c4 + (i & 1);
+          if (head < G) {
+            const int dim = 16 * mt + g + 8 * (i >> 1);
+            comb_o[(warp * G + head) * OP + dim] = o_acc[mt][nt][i];
+          }
+        }
+    if (g == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int head = nt * 8 + 2 * c4 + j;
+          comb_m[warp * HP + head] = m_run[nt][j];
+          comb_l[warp * HP + head] = l_run[nt][j];
+        }
     }
-    o = o / Ls;
-    const float lse = (M + log2f(Ls)) * kLn2;
-    const size_t row = (size_t)b * p.H_q + hkv * G + h;
-    if (final_out) {
-      p.out[row * D + d] = __float2bfloat16(o);
-      if (d == 0 && p.lse_out) p.lse_out[row] = lse;
-    } else {
-      p.o_part[(row * S + split) * D + d] = o;
-      if (d == 0) p.lse_part[row * S + split] = lse;
+    named_bar_sync(1, kConsumerThreads);
+    for (int i = tid; i < G * D; i += kConsumerThreads) {
+      const int h = i / D, d = i - h * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * HP + h]);
+      float Ls = 0.f, o = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float sc = ex2(comb_m[w * HP + h] - M);
+        Ls = fmaf(sc, comb_l[w * HP + h], Ls);
+        o = fmaf(sc, comb_o[(w * G + h) * OP + d], o);
+      }
+      o = o / Ls;
+      const float lse = (M + log2f(Ls)) * kLn2;
+      const size_t row = (size_t)r.b * p.H_q + r.hkv * G + h;
+      if (final_out) {
+        p.out[row * D + d] = __float2bfloat16(o);
+        if (d == 0 && p.lse_out) p.lse_out[row] = lse;
+      } else {
+        p.o_part[(row * S + r.split) * D + d] = o;
+        if (d == 0) p.lse_part[row * S + r.split] = lse;
+      }
     }
+    // the next item's first named barrier orders these reads before reuse
   }
+  if (!ok && lane == 0) report(p.dev_err, INKLING_DEVERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
@@ -613,8 +661,16 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
 // ---------------------------------------------------------------------------
 // Host launcher
 
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 152;
+  return n;
+}
+
 template <int D, int NT, int BH>
-static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int smem_bytes) {
+static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int smem_bytes, int grid) {
   auto kern = decode_kernel<D, NT, BH>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -622,7 +678,6 @@ static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int sme
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (attr_err != cudaSuccess) return INKLING_ERR_CUDA;
-  dim3 grid(c.S, c.H_kv, c.B);
   kern<<<grid, kDecodeThreads, smem_bytes, c.stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return INKLING_ERR_CUDA;
   return INKLING_OK;
@@ -645,6 +700,7 @@ int launch_decode(const DecodeCall& c) {
       return INKLING_ERR_CUDA;
   }
   const int G = c.H_q / c.H_kv;
+  const int NT = (G <= 8) ? 1 : 2;
   prm.q = static_cast<const __nv_bfloat16*>(c.q);
   prm.page_table = c.page_table;
   prm.seq_lens = c.seq_lens;
@@ -654,6 +710,8 @@ int launch_decode(const DecodeCall& c) {
   prm.o_part = c.o_part;
   prm.lse_part = c.lse_part;
   prm.dev_err = c.dev_err;
+  prm.counter = c.counter;
+  prm.B = c.B;
   prm.pt_stride = c.pt_stride;
   prm.H_q = c.H_q;
   prm.H_kv = c.H_kv;
@@ -665,36 +723,48 @@ int launch_decode(const DecodeCall& c) {
   prm.S = c.S;
   prm.chunk = c.chunk;
   prm.scale_log2 = c.scale * kLog2e;
+  prm.total_items = c.B * c.H_kv * c.S;
 
-  // bias entries per head: the widest distance range one CTA can need
-  const int keys_cta = (c.S > 1) ? c.chunk : c.keys_max;
-  prm.nb = std::max(1, std::min(c.R, keys_cta));
-  const int NT = (G <= 8) ? 1 : 2;
-  const int stage_bytes = 2 * (c.D / 64) * kHalfBytes;
-  const int bias_bytes = ((G * prm.nb * 4 + 15) / 16) * 16;
-  // aim at two CTAs per SM; keep 2..4 stages
-  const int budget = 110 * 1024 - bias_bytes - 1024 - 256;
-  int stages = std::max(2, std::min(4, budget / stage_bytes));
-  const int combine_bytes = kConsumerWarps * 8 * NT * (c.D + 4) * 4 + 2 * kConsumerWarps * 8 * NT * 4;
-  while (stages * stage_bytes < combine_bytes) ++stages;
+  // bias entries per head: the widest distance range one item can need
+  const int keys_item = (c.S > 1) ? c.chunk : c.keys_max;
+  int nb = std::max(1, std::min(c.R, keys_item));
+  // kCtasPerSm CTAs per SM: keep each CTA under the budget; 2..max stages
+  const int budget = INKLING_DECODE_SMEM_BUDGET_KB * 1024;
+  int stages = INKLING_DECODE_MAX_STAGES;
+  while (stages > 2 && DecodeSmem(c.D, G, NT, nb, stages).total > budget) --stages;
+  if (DecodeSmem(c.D, G, NT, nb, stages).total > budget) nb = 1;  // bias read through L1/L2
+  prm.nb = nb;
   prm.stages = stages;
-  int smem = 1024 + stages * stage_bytes + bias_bytes + 2 * stages * 8 + 16;
-  if (smem > 227 * 1024) {  // very long bias rows: fall back to reading bias from global
-    prm.nb = 1;
-    smem = 1024 + stages * stage_bytes + 16 + 2 * stages * 8 + 16;
+  const int smem = 1024 + DecodeSmem(c.D, G, NT, nb, stages).total;
+
+  // Static schedule: give every CTA the same number of items (a grid of
+  // ceil(items / waves) CTAs), so the last wave is not a partial one.
+  // Dynamic schedule (splits of uneven length): fill every slot.
+  const int slots = kCtasPerSm * sm_count();
+  int grid = std::min(prm.total_items, slots);
+  if (!c.counter && INKLING_DECODE_BALANCED) {
+    const int waves = (prm.total_items + slots - 1) / slots;
+    grid = (prm.total_items + waves - 1) / waves;
   }
+  grid = std::max(1, grid);
+  if (c.counter && cudaMemsetAsync(c.counter, 0, sizeof(int32_t), c.stream) != cudaSuccess)
+    return INKLING_ERR_CUDA;
 
   int rc;
   if (c.D == 128) {
     if (BH == 64)
-      rc = NT == 1 ? launch_decode_t<128, 1, 64>(c, prm, smem) : launch_decode_t<128, 2, 64>(c, prm, smem);
+      rc = NT == 1 ? launch_decode_t<128, 1, 64>(c, prm, smem, grid)
+                   : launch_decode_t<128, 2, 64>(c, prm, smem, grid);
     else
-      rc = NT == 1 ? launch_decode_t<128, 1, 16>(c, prm, smem) : launch_decode_t<128, 2, 16>(c, prm, smem);
+      rc = NT == 1 ? launch_decode_t<128, 1, 16>(c, prm, smem, grid)
+                   : launch_decode_t<128, 2, 16>(c, prm, smem, grid);
   } else {
     if (BH == 64)
-      rc = NT == 1 ? launch_decode_t<64, 1, 64>(c, prm, smem) : launch_decode_t<64, 2, 64>(c, prm, smem);
+      rc = NT == 1 ? launch_decode_t<64, 1, 64>(c, prm, smem, grid)
+                   : launch_decode_t<64, 2, 64>(c, prm, smem, grid);
     else
-      rc = NT == 1 ? launch_decode_t<64, 1, 16>(c, prm, smem) : launch_decode_t<64, 2, 16>(c, prm, smem);
+      rc = NT == 1 ? launch_decode_t<64, 1, 16>(c, prm, smem, grid)
+                   : launch_decode_t<64, 2, 16>(c, prm, smem, grid);
   }
   if (rc != INKLING_OK || c.S <= 1) return rc;
 

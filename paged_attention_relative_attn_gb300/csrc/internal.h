@@ -28,6 +28,7 @@ struct DecodeCall {
   float* lse_out;
   float* o_part;     // [B, H_q, S, D] when S > 1
   float* lse_part;   // [B, H_q, S]   when S > 1
+  int32_t* counter;  // work-item counter (S > 1), zeroed by the launcher
   int32_t* dev_err;
   cudaStream_t stream;
 };

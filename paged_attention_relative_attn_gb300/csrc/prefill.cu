@@ -1,9 +1,661 @@
-// Chunked / paged prefill (placeholder until the tcgen05 kernel lands).
+// Chunked / paged prefill with a learned relative-position bias on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Operation: inkling_rel_attn_prefill in include/inkling_rel_attn.h (Support
+// Inkling-NVFP4 model, TensorRT-LLM PR #17062, "Implementation": paged prefill
+// applying the relative bias to the scores; "Architecture": bias per (query
+// token, head, relative distance), sliding window 512 / full causal).
+//
+// One CTA per (128-query tile of one sequence, query head), 6 warps:
+//  * warp 0 loads the Q tile once (TMA) and walks the tile's visible key range
+//    in page-respecting tiles of 64 keys (TMA of K and V, 128-byte swizzle,
+//    2-stage ring), exactly like the decode kernel;
+//  * warp 1 owns tensor memory (S double buffer 2 x 64 columns + O, D columns)
+//    and one of its threads issues the MMAs: S_k = Q K_k^T (A and B from shared
+//    memory, K-major) and O += P_{k-1} V_{k-1} (A = P from tensor memory, B = V
+//    MN-major from shared memory), so QK^T of tile k overlaps the softmax of
+//    tile k-1;
+//  * warps 2-5 are the softmax warpgroup: thread = one query row = one TMEM
+//    lane.  They read S with tcgen05.ld, add the bias, apply the causal /
+//    window mask, keep the running max lazily (O is rescaled in tensor memory
+//    only when the max grows by more than 2^8), write P (bf16) back into the S
+//    columns with tcgen05.st, and finally normalise O and store it.
+//
+// The bias (the dominant HBM stream: every query row reads its own band of
+// rel_logits, 64 distances per key tile, each element exactly once) is
+// prefetched two tiles ahead by the softmax warps with 16-byte cp.async into
+// per-row shared-memory bands.  Rows are assigned to TMEM lanes interleaved by
+// four (lane y of lane group j holds query row j + 4y; Q is loaded in that row
+// order by four TMA maps, one per token residue mod 4), so that within a warp
+// every row's band has the same alignment and is read with conflict-free
+// 16-byte shared loads.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
 #include "internal.h"
+#include "plan.cuh"
+#include "ptx.cuh"
+#include "tc.cuh"
 
 namespace ira {
-int launch_prefill(const PrefillCall& c) {
-  (void)c;
-  return INKLING_ERR_CUDA;
+
+constexpr int kPrefThreads = 192;
+constexpr int kQRows = 128;
+constexpr int kKvStages = 2;
+constexpr int kBiasBufs = 3;
+constexpr int kBiasPitch = 68;                       // floats per row band (64 + alignment)
+constexpr int kBiasWarpBytes = 32 * kBiasPitch * 4;  // 32 rows of one warp
+constexpr int kBiasBufBytes = 4 * kBiasWarpBytes;    // 128 rows
+constexpr float kRescaleThreshold = 8.0f;            // log2 units: rescale O when max grows > 2^8
+
+struct PrefillParams {
+  CUtensorMap tmap_q[4];  // tokens r + 4y of q: {D, H_q, y}, box {64, 1, 32}
+  CUtensorMap tmap_k;     // [num_pages][P][H_kv][D] bf16, box {64, 1, BH, 1}
+  CUtensorMap tmap_v;
+  const float* rel;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  __nv_bfloat16* out;
+  float* lse_out;
+  int32_t* dev_err;
+  int B, T, H_q, H_kv, G, P, num_pages, R, window, pt_stride, tiles_per_seq, max_q_len;
+  float scale_log2;
+};
+
+template <int D>
+struct PrefillSmem {
+  static constexpr int HALVES = D / 64;
+  static constexpr int QHALF = kQRows * 128;
+  static constexpr int Q_BYTES = HALVES * QHALF;
+  static constexpr int TILE_BYTES = HALVES * kHalfBytes;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int KV_OFF = Q_BYTES;
+  static constexpr int BIAS_OFF = KV_OFF + kKvStages * STAGE_BYTES;
+  static constexpr int BAR_OFF = BIAS_OFF + kBiasBufs * kBiasBufBytes;
+  // q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done
+  static constexpr int NBARS = 1 + 2 * kKvStages + 2 + 2 + 1;
+  static constexpr int TOTAL = BAR_OFF + NBARS * 8 + 16;
+};
+
+// Bias + scale + mask of one 64-key tile for one query row.  OFF is the
+// warp-uniform alignment of the row's band in shared memory: the bias of key
+// column c sits at float OFF + 63 - c of the band.
+template <int OFF>
+__device__ __forceinline__ void score_tile(float (&s)[64], const uint32_t (&sraw)[2][32],
+                                           const float* band, float sl2, int cl, int ch,
+                                           bool full_vis, bool clamp, int dtop, int Rm1,
+                                           float clampv) {
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float bb[36];
+    const float4* src = reinterpret_cast<const float4*>(band) + (hh == 0 ? 8 : 0);
+#pragma unroll
+    for (int q = 0; q < 9; ++q) {
+      const float4 v = src[q];
+      bb[4 * q + 0] = v.x;
+      bb[4 * q + 1] = v.y;
+      bb[4 * q + 2] = v.z;
+      bb[4 * q + 3] = v.w;
+    }
+#pragma unroll
+    for (int cc = 0; cc < 32; ++cc) {
+      const int c = 32 * hh + cc;
+      const int idx = OFF + 63 - c - (hh == 0 ? 32 : 0);
+      float bv = bb[idx] * kLog2e;
+      if (clamp) bv = (dtop - c >= Rm1) ? clampv : bv;
+      float v = fmaf(__uint_as_float(sraw[hh][cc]), sl2, bv);
+      if (!full_vis) v = (c >= cl && c <= ch) ? v : -INFINITY;
+      s[c] = v;
+    }
+  }
 }
+
+template <int D, int BH>
+__global__ void __launch_bounds__(kPrefThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using SM = PrefillSmem<D>;
+  constexpr int HALVES = SM::HALVES;
+  constexpr int TILE_BYTES = SM::TILE_BYTES;
+  constexpr uint32_t kTmemCols = 256;  // S0 [0,64) S1 [64,128) O [128, 128+D)
+  constexpr uint32_t kOCol = 128;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int h = blockIdx.x;
+  const int b = blockIdx.y / p.tiles_per_seq;
+  const int qt = blockIdx.y - b * p.tiles_per_seq;
+  if (b >= p.B) return;
+
+  // ---- the query tile and its key range (identical in every thread)
+  const int tb = p.cu_seqlens_q[b];
+  const int q_len = p.cu_seqlens_q[b + 1] - tb;
+  if (q_len <= 0 || qt * kQRows >= q_len) return;
+  int L = p.seq_lens[b];
+  const int cap = p.pt_stride * p.P;
+  if (L > cap) {
+    if (tid == 0 && h == 0 && qt == 0) report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
+    L = cap;
+  }
+  if (q_len > L || tb < 0 || tb + q_len > p.T) {
+    if (tid == 0 && h == 0 && qt == 0) report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);
+    return;
+  }
+  if (q_len > p.max_q_len && tid == 0 && h == 0 && qt == 0)
+    report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);  // tiles past the grid are not computed
+  const int t0 = tb + qt * kQRows;
+  const int nrows = min(kQRows, q_len - qt * kQRows);
+  const int pos0 = L - q_len + qt * kQRows;  // position of row 0
+  const int khi_all = pos0 + nrows - 1;
+  const int klo_all = p.window > 0 ? max(0, pos0 - p.window + 1) : 0;
+  const int hkv = h / p.G;
+  const int R = p.R;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + kKvStages;
+  uint64_t* s_full = kv_empty + kKvStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (tid == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(smem_u32(&kv_full[s]), 1);
+      mbar_init(smem_u32(&kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&s_full[s]), 1);
+      mbar_init(smem_u32(&p_full[s]), 4);
+    }
+    mbar_init(smem_u32(pv_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // =================================================================== loader
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int r = 0; r < 4; ++r) tmap_prefetch(&p.tmap_q[r]);
+      tmap_prefetch(&p.tmap_k);
+      tmap_prefetch(&p.tmap_v);
+      // Q tile: row group j (rows j + 4y) = tokens t0 + j + 4y
+      int ngroups = 0;
+      for (int j = 0; j < 4; ++j) ngroups += (j < nrows) ? 1 : 0;
+      const uint64_t pol_q = policy_evict_first();
+      mbar_arrive_expect_tx(smem_u32(q_full), ngroups * HALVES * 32 * 128);
+      for (int j = 0; j < 4; ++j) {
+        if (j >= nrows) continue;
+        const int tok = t0 + j;
+        for (int hh = 0; hh < HALVES; ++hh)
+          tma_load_3d(smem_u32(smem + hh * SM::QHALF + 32 * j * 128), &p.tmap_q[tok & 3],
+                      smem_u32(q_full), hh * 64, h, tok >> 2, pol_q);
+      }
+    }
+    const uint64_t pol_kv = policy_evict_last();
+    const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride;
+    int batch_base = -1000000;
+    int my_page = 0;
+    auto page_of = [&](int lp) -> int {  // warp-uniform
+      if (lp < batch_base || lp >= batch_base + 32) {
+        batch_base = lp;
+        const int idx = lp + lane;
+        my_page = (idx < p.pt_stride) ? __ldg(pt_row + idx) : 0;
+      }
+      return __shfl_sync(0xffffffffu, my_page, lp - batch_base);
+    };
+    int kt = 0;
+    bool ok = true;
+    if constexpr (BH == 64) {
+      PlanBig plan(klo_all, khi_all, p.P);
+      while (!plan.done()) {
+        const int st = kt % kKvStages;
+        if (kt >= kKvStages && lane == 0)
+          ok = mbar_wait(smem_u32(&kv_empty[st]), ((kt / kKvStages) - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        int lp, slot0;
+        plan.next(lp, slot0);
+        const int page = page_of(lp);
+        if (lane == 0) {
+          if (page < 0 || page >= p.num_pages) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+          const uint32_t kdst = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES);
+          const uint32_t vdst = kdst + TILE_BYTES;
+          const uint32_t fb = smem_u32(&kv_full[st]);
+          mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
+          for (int hh = 0; hh < HALVES; ++hh) {
+            tma_load_4d(kdst + hh * kHalfBytes, &p.tmap_k, fb, hh * 64, hkv, slot0, page, pol_kv);
+            tma_load_4d(vdst + hh * kHalfBytes, &p.tmap_v, fb, hh * 64, hkv, slot0, page, pol_kv);
+          }
+        }
+        __syncwarp();
+        ++kt;
+      }
+    } else {
+      PlanSmall plan(klo_all, khi_all);
+      while (!plan.done()) {
+        const int st = kt % kKvStages;
+        if (kt >= kKvStages && lane == 0)
+          ok = mbar_wait(smem_u32(&kv_empty[st]), ((kt / kKvStages) - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const Tile t = plan.next();
+        int nbox = 0;
+        int pages[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int k0 = t.jbase + 16 * c;
+          const bool need = (k0 <= t.khi) && (k0 + 15 >= t.klo);
+          pages[c] = need ? page_of(k0 / p.P) : 0;
+          nbox += need ? 1 : 0;
+        }
+        if (lane == 0) {
+          const uint32_t kdst = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES);
+          const uint32_t vdst = kdst + TILE_BYTES;
+          const uint32_t fb = smem_u32(&kv_full[st]);
+          mbar_arrive_expect_tx(fb, nbox * 2 * HALVES * 16 * 128);
+          for (int c = 0; c < 4; ++c) {
+            const int k0 = t.jbase + 16 * c;
+            if (!((k0 <= t.khi) && (k0 + 15 >= t.klo))) continue;
+            if (pages[c] < 0 || pages[c] >= p.num_pages) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+            for (int hh = 0; hh < HALVES; ++hh) {
+              tma_load_4d(kdst + hh * kHalfBytes + c * 16 * 128, &p.tmap_k, fb, hh * 64, hkv,
+                          k0 % p.P, pages[c], pol_kv);
+              tma_load_4d(vdst + hh * kHalfBytes + c * 16 * 128, &p.tmap_v, fb, hh * 64, hkv,
+                          k0 % p.P, pages[c], pol_kv);
+            }
+          }
+        }
+        __syncwarp();
+        ++kt;
+      }
+    }
+    if (!ok && lane == 0) {
+      report(p.dev_err, INKLING_DEVERR_TIMEOUT);
+      for (int j = max(0, kt - kKvStages); j < kt; ++j)
+        mbar_wait_drain(smem_u32(&kv_full[j % kKvStages]), (j / kKvStages) & 1);
+      mbar_wait_drain(smem_u32(q_full), 0);
+    }
+  }
+  // =================================================================== MMA issuer
+  else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kQRows, kTileRows, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(kQRows, D, true);
+      const uint32_t q_base = smem_u32(smem);
+      bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag);
+      tc_fence_after();
+      int issued_pv = 0;  // PV MMAs issued (== completed phases of pv_done once waited)
+      auto issue_pv = [&](int kp) -> bool {
+        if (!mbar_wait(smem_u32(&p_full[kp & 1]), (kp >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const int st = kp % kKvStages;
+        const uint32_t vb = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES) + TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
+          tc_mma_ts(tmem + kOCol, tmem + 64 * (kp & 1) + 8 * kk, bdesc, idesc_pv,
+                    (kp > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(pv_done));
+        tc_commit(smem_u32(&kv_empty[st]));
+        ++issued_pv;
+        return true;
+      };
+      int k = 0;
+      if (ok) {
+        // walk the same tiles as the loader (only the count matters here)
+        int ntiles = 0;
+        if constexpr (BH == 64) {
+          PlanBig plan(klo_all, khi_all, p.P);
+          int lp, s0;
+          while (!plan.done()) {
+            plan.next(lp, s0);
+            ++ntiles;
+          }
+        } else {
+          PlanSmall plan(klo_all, khi_all);
+          while (!plan.done()) {
+            plan.next();
+            ++ntiles;
+          }
+        }
+        for (k = 0; k < ntiles && ok; ++k) {
+          const int st = k % kKvStages;
+          ok = mbar_wait(smem_u32(&kv_full[st]), (k / kKvStages) & 1, abort_flag);
+          if (!ok) break;
+          if (k >= 2) {  // S buffer k&1 is free once PV_{k-2} has read P_{k-2}
+            ok = mbar_wait(smem_u32(pv_done), (k - 2) & 1, abort_flag);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          const uint32_t kb = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t adesc =
+                smem_desc_sw128(q_base + (kk >> 2) * SM::QHALF + (kk & 3) * 32, 16, 1024);
+            const uint64_t bdesc =
+                smem_desc_sw128(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+            tc_mma_ss(tmem + 64 * (k & 1), adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&s_full[k & 1]));
+          if (k >= 1) ok = issue_pv(k - 1);
+        }
+        if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
+      }
+      if (!ok) {
+        report(p.dev_err, INKLING_DEVERR_TIMEOUT);
+        // let the MMAs already issued finish before tensor memory is released
+        if (issued_pv > 0) mbar_wait_drain(smem_u32(pv_done), (issued_pv - 1) & 1);
+      }
+    }
+    __syncwarp();
+  }
+  // =================================================================== softmax
+  else {
+    const int lg = warp & 3;         // TMEM lane group of this warp
+    const int i = lg + 4 * lane;     // query row of this thread within the tile
+    const bool valid = i < nrows;
+    const int pi = pos0 + i;         // its absolute position
+    const int lo_i = p.window > 0 ? max(0, pi - p.window + 1) : 0;
+    const size_t row_off = ((size_t)(valid ? t0 + i : t0) * p.H_q + h) * R;
+    const float clampv = valid ? __ldg(p.rel + row_off + R - 1) * kLog2e : 0.f;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * lg) << 16);
+    const float sl2 = p.scale_log2;
+    const uint64_t pol_b = policy_evict_first();
+    float* band_base = reinterpret_cast<float*>(smem + SM::BIAS_OFF) + lg * 32 * kBiasPitch;
+    const float* my_band0 = band_base + lane * kBiasPitch;
+
+    // copy this warp's 32 row bands of one tile into bias buffer `buf`
+    auto issue_bias = [&](const Tile& t, int buf) {
+      const uint32_t dst0 = smem_u32(band_base) + buf * kBiasBufBytes;
+#pragma unroll 4
+      for (int it = 0; it < 17; ++it) {
+        int yy, c;
+        if (it < 16) {
+          yy = 2 * it + (lane >> 4);
+          c = lane & 15;
+        } else {
+          yy = lane;
+          c = 16;
+        }
+        const int ii = lg + 4 * yy;
+        if (ii >= nrows) continue;
+        const int pp = pos0 + ii;
+        const int lo_r = p.window > 0 ? max(0, pp - p.window + 1) : 0;
+        const int vlo = max(lo_r, t.klo), vhi = min(pp, t.khi);
+        if (vlo > vhi) continue;
+        const int dtop = pp - t.jbase;
+        const int d0 = ((dtop - 63) & ~3) + 4 * c;
+        const int dmin = pp - vhi, dmax = min(pp - vlo, R - 1);
+        if (d0 + 3 < dmin || d0 > dmax) continue;
+        const float* src = p.rel + ((size_t)(t0 + ii) * p.H_q + h) * R + d0;
+        asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                         dst0 + (uint32_t)(yy * kBiasPitch * 4 + c * 16)),
+                     "l"(src), "l"(pol_b)
+                     : "memory");
+      }
+    };
+
+    // walk tiles: `cur` for the compute, `pre` two tiles ahead for the bias prefetch
+    using PlanT = typename std::conditional<BH == 64, PlanBig, PlanSmall>::type;
+    auto make_plan = [&]() {
+      if constexpr (BH == 64) return PlanBig(klo_all, khi_all, p.P);
+      else return PlanSmall(klo_all, khi_all);
+    };
+    auto next_tile = [&](PlanT& pl) -> Tile {
+      if constexpr (BH == 64) {
+        int lp, s0;
+        return pl.next(lp, s0);
+      } else {
+        return pl.next();
+      }
+    };
+    PlanT cur = make_plan();
+    PlanT pre = make_plan();
+    for (int j = 0; j < 2; ++j) {  // bias of tiles 0 and 1
+      if (!pre.done()) issue_bias(next_tile(pre), j);
+      cp_async_commit();
+    }
+
+    float m_use = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    int k = 0;
+    for (; !cur.done(); ++k) {
+      const Tile t = next_tile(cur);
+      if (!pre.done()) issue_bias(next_tile(pre), (k + 2) % kBiasBufs);
+      cp_async_commit();
+
+      if (!mbar_wait_warp(smem_u32(&s_full[k & 1]), (k >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sraw[2][32];
+      tmem_ld32(tlane + 64 * (k & 1), sraw[0]);
+      tmem_ld32(tlane + 64 * (k & 1) + 32, sraw[1]);
+      tmem_ld_wait();
+      cp_async_wait<2>();
+      __syncwarp();
+
+      int cl = max(lo_i, t.klo) - t.jbase;
+      int ch = min(pi, t.khi) - t.jbase;
+      if (!valid) {
+        cl = 64;
+        ch = -1;
+      }
+      const int dtop = pi - t.jbase;
+      const bool full_vis = __all_sync(0xffffffffu, cl <= 0 && ch >= 63);
+      const bool clamp = __any_sync(0xffffffffu, valid && cl <= ch && dtop - cl >= R - 1);
+      const int off = (pos0 + lg - t.jbase - 63) & 3;
+      const float* band = my_band0 + (k % kBiasBufs) * (kBiasBufBytes / 4);
+      float s[64];
+      switch (off) {
+        case 0: score_tile<0>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        case 1: score_tile<1>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        case 2: score_tile<2>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        default: score_tile<3>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+      }
+
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+      float m_new = m_use, alpha = 1.f;
+      bool resc = false;
+      if (mx > -INFINITY) {
+        if (m_use == -INFINITY) {
+          m_new = mx;  // first visible keys of this row: its O row is still zero
+        } else if (mx > m_use + kRescaleThreshold) {
+          m_new = mx;
+          alpha = ex2(m_use - mx);
+          resc = true;
+        }
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // O holds PV_0..PV_{k-1}; wait for the last one, then rescale in place
+        if (!mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tlane + kOCol + 32 * cc, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          tmem_st32(tlane + kOCol + 32 * cc, o);
+        }
+        tmem_st_wait();
+      }
+      m_use = m_new;
+      l_sum *= alpha;
+      const float mu = (m_use == -INFINITY) ? 0.f : m_use;
+      uint32_t pk[32];
+      float sum = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const float p0 = ex2(s[2 * m] - mu);
+        const float p1 = ex2(s[2 * m + 1] - mu);
+        sum += p0 + p1;
+        pk[m] = pack_bf16(p0, p1);
+      }
+      l_sum += sum;
+      tmem_st32(tlane + 64 * (k & 1), pk);
+      tmem_st_wait();
+
+      if (t.dirty) {
+        // rows outside [klo, khi] may hold other keys' values (NaN included):
+        // zero them in V so that P = 0 times V stays 0 in the tensor core
+        const int vlo = t.klo - t.jbase, vhi = t.khi - t.jbase;
+        const int st = k % kKvStages;
+        uint8_t* vtile = smem + SM::KV_OFF + st * SM::STAGE_BYTES + TILE_BYTES;
+        const int sid = (warp - 2) * 32 + lane;  // 0..127
+        for (int u = sid; u < 64 * HALVES * 8; u += 128) {
+          const int row = u / (HALVES * 8);
+          const int rest = u - row * HALVES * 8;
+          if (row >= vlo && row <= vhi) continue;
+          *reinterpret_cast<uint4*>(vtile + (rest >> 3) * kHalfBytes + row * 128 + (rest & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[k & 1]));
+    }
+    cp_async_wait<0>();
+
+    // ---- epilogue: O / l -> bf16
+    if (ok && k > 0) ok = mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      __nv_bfloat16* orow = p.out + ((size_t)(t0 + i) * p.H_q + h) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tlane + kOCol + 32 * cc, o);
+        tmem_ld_wait();
+        if (valid) {
+          uint32_t pkd[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            pkd[x] = pack_bf16(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
+        }
+      }
+      if (valid && p.lse_out)
+        p.lse_out[(size_t)(t0 + i) * p.H_q + h] =
+            l_sum > 0.f ? (m_use + log2f(l_sum)) * kLn2 : -INFINITY;
+    } else if (lane == 0) {
+      report(p.dev_err, INKLING_DEVERR_TIMEOUT);
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host launcher
+
+template <int D, int BH>
+static int launch_prefill_t(const PrefillCall& c, const PrefillParams& prm, dim3 grid) {
+  auto kern = prefill_kernel<D, BH>;
+  const int smem = 1024 + PrefillSmem<D>::TOTAL;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return INKLING_ERR_CUDA;
+  kern<<<grid, kPrefThreads, smem, c.stream>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return INKLING_ERR_CUDA;
+  return INKLING_OK;
+}
+
+int launch_prefill(const PrefillCall& c) {
+  PrefillParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int BH = (c.P % 64 == 0) ? 64 : 16;
+  const uint64_t tok_bytes = (uint64_t)c.H_q * c.D * 2;
+  for (int r = 0; r < 4; ++r) {
+    const uint64_t rows = c.T > r ? (uint64_t)(c.T - r + 3) / 4 : 1;
+    uint64_t dims[3] = {(uint64_t)c.D, (uint64_t)c.H_q, rows};
+    uint64_t strides[2] = {(uint64_t)c.D * 2, 4 * tok_bytes};
+    uint32_t box[3] = {64, 1, 32};
+    const char* base = static_cast<const char*>(c.q) + (c.T > r ? r : 0) * tok_bytes;
+    if (!encode_tiled(&prm.tmap_q[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<char*>(base),
+                      dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return INKLING_ERR_CUDA;
+  }
+  {
+    uint64_t dims[4] = {(uint64_t)c.D, (uint64_t)c.H_kv, (uint64_t)c.P, (uint64_t)c.num_pages};
+    uint64_t strides[3] = {(uint64_t)c.D * 2, (uint64_t)c.H_kv * c.D * 2,
+                           (uint64_t)c.P * c.H_kv * c.D * 2};
+    uint32_t box[4] = {64, 1, (uint32_t)BH, 1};
+    if (!encode_tiled(&prm.tmap_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(c.k_cache),
+                      dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return INKLING_ERR_CUDA;
+    if (!encode_tiled(&prm.tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(c.v_cache),
+                      dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return INKLING_ERR_CUDA;
+  }
+  prm.rel = c.rel;
+  prm.cu_seqlens_q = c.cu_seqlens_q;
+  prm.seq_lens = c.seq_lens;
+  prm.page_table = c.page_table;
+  prm.out = static_cast<__nv_bfloat16*>(c.out);
+  prm.lse_out = c.lse_out;
+  prm.dev_err = c.dev_err;
+  prm.B = c.B;
+  prm.T = c.T;
+  prm.H_q = c.H_q;
+  prm.H_kv = c.H_kv;
+  prm.G = c.H_q / c.H_kv;
+  prm.P = c.P;
+  prm.num_pages = c.num_pages;
+  prm.R = c.R;
+  prm.window = c.window;
+  prm.pt_stride = c.pt_stride;
+  prm.max_q_len = c.max_q_len;
+  prm.tiles_per_seq = std::max(1, (c.max_q_len + kQRows - 1) / kQRows);
+  prm.scale_log2 = c.scale * kLog2e;
+  if (c.max_q_len <= 0) return INKLING_OK;
+  dim3 grid(c.H_q, c.B * prm.tiles_per_seq);
+  if (c.D == 128)
+    return BH == 64 ? launch_prefill_t<128, 64>(c, prm, grid) : launch_prefill_t<128, 16>(c, prm, grid);
+  return BH == 64 ? launch_prefill_t<64, 64>(c, prm, grid) : launch_prefill_t<64, 16>(c, prm, grid);
+}
+
 }  // namespace ira

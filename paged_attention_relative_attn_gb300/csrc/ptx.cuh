@@ -69,6 +69,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
 }
+// Warp-collective bounded wait: every lane observes the phase completion
+// itself (so data the phase publishes, e.g. TMA writes, is visible to every
+// lane); the result is the same in all lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const unsigned long long t0 = globaltimer();
+  const bool leader = (threadIdx.x & 31) == 0;
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if ((it & 31u) == 0) {
+      int stop = 0;
+      if (leader) {
+        if (*abort) {
+          stop = 1;
+        } else if (globaltimer() - t0 > kWaitTimeoutNs) {
+          *abort = 1;
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+}
 // Bounded wait that ignores the abort flag (used to drain copies in flight).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();

@@ -72,10 +72,10 @@ def test_workspace_size(lib):
     rows = 32 * 48 * S
     r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert (lib.inkling_rel_attn_decode_workspace_size(32, 48, 8, 128, 0, 32768, 0, 152)
-            == r256(rows * 128 * 4) + r256(rows * 4))
+            == 256 + r256(rows * 128 * 4) + r256(rows * 4))
     # forced splits are clamped to one per 64 keys
     assert lib.inkling_rel_attn_decode_workspace_size(1, 4, 2, 64, 0, 100, 50, 152) == \
-        r256(1 * 4 * 2 * 64 * 4) + r256(1 * 4 * 2 * 4)
+        256 + r256(1 * 4 * 2 * 64 * 4) + r256(1 * 4 * 2 * 4)
     assert lib.inkling_rel_attn_prefill_workspace_size(8192, 48, 128) == 0
 
 
