@@ -48,12 +48,12 @@ namespace ira {
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kDecodeThreads = kConsumerThreads + 32;
-constexpr int kItemSlots = 4;
+constexpr int kItemSlots = 3;
 #ifndef INKLING_DECODE_CTAS_PER_SM
 #define INKLING_DECODE_CTAS_PER_SM 2
 #endif
 #ifndef INKLING_DECODE_SMEM_BUDGET_KB
-#define INKLING_DECODE_SMEM_BUDGET_KB 110
+#define INKLING_DECODE_SMEM_BUDGET_KB 111
 #endif
 #ifndef INKLING_DECODE_MAX_STAGES
 #define INKLING_DECODE_MAX_STAGES 4
@@ -77,8 +77,8 @@ struct DecodeParams {
   int32_t* dev_err;
   int32_t* counter;  // dynamic scheduling (zeroed before launch), or nullptr
   int B, pt_stride, H_q, H_kv, G, P, num_pages, R, window;
-  int S, chunk, stages, nb;
-  int total_items;
+  int S, chunk, stages;
+  int bias_prefetch;  // rel_logits rows are 16-byte aligned: L2 prefetch allowed
   float scale_log2;
 };
 
@@ -111,16 +111,16 @@ struct ItemRec {
 // Shared-memory layout (byte offsets from the 1024-aligned base), computed
 // identically on host and device.
 struct DecodeSmem {
-  int stage_bytes, stages, bias_off, comb_off, ring_off, bar_off, total;
-  __host__ __device__ DecodeSmem(int D, int G, int NT, int nb, int stages_) {
+  int stage_bytes, stages, slot_bytes, ring_off, comb_off, pre_off, bar_off, total;
+  __host__ __device__ DecodeSmem(int D, int G, int NT, int stages_, int n_prefix) {
     stage_bytes = 2 * (D / 64) * kHalfBytes;
     stages = stages_;
-    bias_off = stages * stage_bytes;
-    const int bias_bytes = ((G * nb * 4 + 127) / 128) * 128;
-    comb_off = bias_off + bias_bytes;
+    slot_bytes = 128 + ((G * D * 2 + 127) / 128) * 128;  // item record + q rows
+    ring_off = stages * stage_bytes;
+    comb_off = ring_off + kItemSlots * slot_bytes;
     const int comb_bytes = kConsumerWarps * G * (D + 4) * 4 + 2 * kConsumerWarps * 8 * NT * 4;
-    ring_off = comb_off + ((comb_bytes + 127) / 128) * 128;
-    bar_off = ring_off + kItemSlots * (int)sizeof(ItemRec);
+    pre_off = comb_off + ((comb_bytes + 127) / 128) * 128;
+    bar_off = pre_off + ((n_prefix * 4 + 127) / 128) * 128;
     total = bar_off + (2 * stages + 2 * kItemSlots) * 8 + 16;
   }
 };
@@ -142,20 +142,22 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   const int lane = tid & 31;
   const int G = p.G;
   const int S = p.S;
-  const DecodeSmem L(D, G, NT, p.nb, p.stages);
+  const bool dense = S > 1;  // items enumerated through a per-sequence prefix sum
+  const DecodeSmem L(D, G, NT, p.stages, dense ? p.B + 1 : 0);
   const int stages = L.stages;
   const int STAGE_BYTES = L.stage_bytes;
 
-  float* bias_s = reinterpret_cast<float*>(smem + L.bias_off);
   float* comb_o = reinterpret_cast<float*>(smem + L.comb_off);  // [4][G][D+4]
   float* comb_m = comb_o + kConsumerWarps * G * (D + 4);          // [4][HP]
   float* comb_l = comb_m + kConsumerWarps * HP;                   // [4][HP]
-  ItemRec* ring = reinterpret_cast<ItemRec*>(smem + L.ring_off);
+  int* prefix = reinterpret_cast<int*>(smem + L.pre_off);         // [B+1] items before b
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  // full[s] = bars[s], empty[s] = bars[stages+s]; item ring barriers after
-  uint64_t* ifull = bars + 2 * stages;
-  uint64_t* iempty = ifull + kItemSlots;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(iempty + kItemSlots);
+  // full[s] = bars[s], empty[s] = bars[stages + s]; item ring after
+  uint64_t* rfull = bars + 2 * stages;
+  uint64_t* rempty = rfull + kItemSlots;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(rempty + kItemSlots);
+  auto slot_rec = [&](int s) { return reinterpret_cast<ItemRec*>(smem + L.ring_off + s * L.slot_bytes); };
+  auto slot_q = [&](int s) { return smem + L.ring_off + s * L.slot_bytes + 128; };
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -163,8 +165,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       mbar_init(smem_u32(&bars[stages + s]), kConsumerWarps);
     }
     for (int i = 0; i < kItemSlots; ++i) {
-      mbar_init(smem_u32(&ifull[i]), 1);
-      mbar_init(smem_u32(&iempty[i]), kConsumerWarps);
+      mbar_init(smem_u32(&rfull[i]), 1);
+      mbar_init(smem_u32(&rempty[i]), kConsumerWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -178,140 +180,254 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       tmap_prefetch(&p.tmap_v);
     }
     const uint64_t pol = policy_evict_first();
-    int kt = 0;  // tiles issued (global over items)
-    int ki = 0;  // items published
-    bool ok = true;
-    for (int n = 0;; ++n) {
-      int id = 0;
+
+    // dense item space: prefix[b] = items of sequences < b (H_kv * max(n_s, 1) each)
+    int total = p.B * p.H_kv;
+    if (dense) {
+      int carry = 0;
+      for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int cnt = 0;
+        if (b < p.B) {
+          const SeqPlan sp = seq_plan(__ldg(p.seq_lens + b), p.pt_stride, p.P, p.window, p.chunk, S);
+          cnt = p.H_kv * max(sp.n_s, 1);
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        if (b < p.B) prefix[b] = carry + incl - cnt;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) prefix[p.B] = carry;
+      total = carry;
+      __syncwarp();
+    }
+
+    // item id -> (b, hkv, split) and its key range
+    auto locate = [&](int id, int& b, int& hkv, int& split) {
+      if (dense) {
+        int lo = 0, hi = p.B - 1;  // last b with prefix[b] <= id
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= id) lo = mid;
+          else hi = mid - 1;
+        }
+        b = lo;
+        const int rest = id - prefix[b];
+        const int nsb = (prefix[b + 1] - prefix[b]) / p.H_kv;
+        hkv = rest / nsb;
+        split = rest - hkv * nsb;
+      } else {
+        b = id / p.H_kv;
+        hkv = id - b * p.H_kv;
+        split = 0;
+      }
+    };
+    int n_static = 0;
+    auto next_id = [&]() -> int {
+      int id;
       if (p.counter) {
+        id = 0;
         if (lane == 0) id = atomicAdd(p.counter, 1);
         id = __shfl_sync(0xffffffffu, id, 0);
       } else {
-        id = blockIdx.x + n * gridDim.x;
+        id = blockIdx.x + (n_static++) * gridDim.x;
       }
+      return id;
+    };
+    auto resolve = [&](int id, int Lraw) -> ItemRec {
       ItemRec r;
       r.b = -1;
       r.hkv = r.split = r.n_s = r.a = r.e = r.pos = r.nvis = 0;
-      if (id < p.total_items) {
-        r.split = id % S;
-        const int rest = id / S;
-        r.hkv = rest % p.H_kv;
-        r.b = rest / p.H_kv;
-        const int Lraw = __ldg(p.seq_lens + r.b);
-        const SeqPlan sp = seq_plan(Lraw, p.pt_stride, p.P, p.window, p.chunk, S);
-        if (r.split >= max(sp.n_s, 1)) continue;  // empty split: nothing to do
-        if (Lraw > p.pt_stride * p.P && lane == 0 && r.hkv == 0 && r.split == 0)
-          report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
-        r.n_s = sp.n_s;
-        r.pos = sp.pos;
-        r.nvis = sp.nvis;
-        r.a = sp.lo + r.split * p.chunk;
-        r.e = (r.split == sp.n_s - 1) ? sp.pos : r.a + p.chunk - 1;
-      }
-      // publish the item
-      {
-        const int slot = ki % kItemSlots;
-        if (ki >= kItemSlots && lane == 0)
-          ok = mbar_wait(smem_u32(&iempty[slot]), ((ki / kItemSlots) - 1) & 1, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane == 0) {
-          ring[slot] = r;
-          mbar_arrive(smem_u32(&ifull[slot]));
-        }
-        ++ki;
-      }
-      if (r.b < 0) break;
-      if (r.nvis == 0) continue;
+      if (id >= total) return r;
+      locate(id, r.b, r.hkv, r.split);
+      const SeqPlan sp = seq_plan(Lraw, p.pt_stride, p.P, p.window, p.chunk, S);
+      if (Lraw > p.pt_stride * p.P && lane == 0 && r.hkv == 0 && r.split == 0)
+        report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
+      r.n_s = sp.n_s;
+      r.pos = sp.pos;
+      r.nvis = sp.nvis;
+      r.a = sp.lo + r.split * p.chunk;
+      r.e = (r.split >= sp.n_s - 1) ? sp.pos : r.a + p.chunk - 1;
+      return r;
+    };
+    auto seq_len_of = [&](int id) -> int {  // issued early, consumed later
+      if (id >= total) return 0;
+      int b, h, s;
+      locate(id, b, h, s);
+      return __ldg(p.seq_lens + b);
+    };
 
-      const int32_t* pt_row = p.page_table + (size_t)r.b * p.pt_stride;
-      int batch_base = -1000000;
-      int my_page = 0;
-      auto page_of = [&](int lp) -> int {  // warp-uniform
-        if (lp < batch_base || lp >= batch_base + 32) {
-          batch_base = lp;
-          const int idx = lp + lane;
-          my_page = (idx < p.pt_stride) ? __ldg(pt_row + idx) : 0;
+    int ki = 0;  // items published
+    bool ok = true;
+    // publish an item: its record and q rows into ring slot ki % kItemSlots,
+    // and a prefetch of its bias rows into L2
+    auto publish = [&](const ItemRec& r) -> bool {
+      const int slot = ki % kItemSlots;
+      bool good = true;
+      if (ki >= kItemSlots && lane == 0)
+        good = mbar_wait(smem_u32(&rempty[slot]), ((ki / kItemSlots) - 1) & 1, abort_flag);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) return false;
+      if (lane == 0) {
+        *slot_rec(slot) = r;
+        const uint32_t fb = smem_u32(&rfull[slot]);
+        if (r.b >= 0 && r.nvis > 0) {
+          const uint32_t qbytes = G * D * 2;
+          mbar_arrive_expect_tx(fb, qbytes);
+          bulk_load(smem_u32(slot_q(slot)), p.q + ((size_t)r.b * p.H_q + r.hkv * G) * D, qbytes, fb);
+        } else {
+          mbar_arrive(fb);
         }
-        return __shfl_sync(0xffffffffu, my_page, lp - batch_base);
+      }
+      if (r.b >= 0 && r.nvis > 0 && p.bias_prefetch && lane < G) {
+        const int dlo = min(r.pos - r.e, p.R - 1) & ~3;
+        const int dhi = min(min(r.pos - r.a, p.R - 1) + 4, p.R) & ~3;
+        const float* row = p.rel + ((size_t)r.b * p.H_q + r.hkv * G + lane) * p.R;
+        if (dhi > dlo) bulk_prefetch_l2(row + dlo, (uint32_t)(dhi - dlo) * 4);
+      }
+      ++ki;
+      return true;
+    };
+
+    // page ids, fetched 32 at a time per item; the next item's first batch is
+    // loaded while the current item's tiles are issued
+    int cur_base = 0, cur_page = 0, nxt_base = 0, nxt_page = 0;
+    const int32_t* cur_row = p.page_table;
+    const int32_t* nxt_row = p.page_table;
+    auto batch_load = [&](const int32_t* row, int base) -> int {
+      const int idx = base + lane;
+      return (idx < p.pt_stride) ? __ldg(row + idx) : 0;
+    };
+    auto page_of = [&](int lp) -> int {  // warp-uniform
+      if (lp < cur_base || lp >= cur_base + 32) {
+        cur_base = lp;
+        cur_page = batch_load(cur_row, lp);
+      }
+      return __shfl_sync(0xffffffffu, cur_page, lp - cur_base);
+    };
+
+    int pid = next_id();
+    int pL = seq_len_of(pid);
+    ItemRec cur = resolve(pid, pL);
+    ok = publish(cur);
+    if (ok && cur.b >= 0) {
+      cur_row = p.page_table + (size_t)cur.b * p.pt_stride;
+      cur_base = cur.a / p.P;
+      cur_page = batch_load(cur_row, cur_base);
+      pid = next_id();
+      pL = seq_len_of(pid);
+    }
+    int kt = 0;  // tiles issued (global over items)
+    while (ok && cur.b >= 0) {
+      ItemRec nxt;
+      bool nxt_done = false;
+      auto do_next = [&]() {  // resolve + publish the following item, prefetch its pages
+        nxt = resolve(pid, pL);
+        ok = publish(nxt);
+        if (ok && nxt.b >= 0) {
+          nxt_row = p.page_table + (size_t)nxt.b * p.pt_stride;
+          nxt_base = nxt.a / p.P;
+          nxt_page = batch_load(nxt_row, nxt_base);
+          pid = next_id();
+          pL = seq_len_of(pid);
+        }
+        nxt_done = true;
       };
-
-      if constexpr (BH == 64) {
-        PlanBig plan(r.a, r.e, p.P);
-        while (!plan.done()) {
-          const int st = kt % stages;
-          if (kt >= stages && lane == 0)
-            ok = mbar_wait(smem_u32(&bars[stages + st]), ((kt / stages) - 1) & 1, abort_flag);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          int lp, slot0;
-          plan.next(lp, slot0);
-          const int page = page_of(lp);
-          if (lane == 0) {
-            if (page < 0 || page >= p.num_pages) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
-            const uint32_t kdst = smem_u32(smem + st * STAGE_BYTES);
-            const uint32_t vdst = kdst + TILE_BYTES;
-            const uint32_t fb = smem_u32(&bars[st]);
-            mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
+      int local = 0;
+      if (cur.nvis > 0) {
+        if constexpr (BH == 64) {
+          PlanBig plan(cur.a, cur.e, p.P);
+          while (!plan.done()) {
+            const int st = kt % stages;
+            if (kt >= stages && lane == 0)
+              ok = mbar_wait(smem_u32(&bars[stages + st]), ((kt / stages) - 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            int lp, slot0;
+            plan.next(lp, slot0);
+            const int page = page_of(lp);
+            if (lane == 0) {
+              if (page < 0 || page >= p.num_pages) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+              const uint32_t kdst = smem_u32(smem + st * STAGE_BYTES);
+              const uint32_t vdst = kdst + TILE_BYTES;
+              const uint32_t fb = smem_u32(&bars[st]);
+              mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
 #pragma unroll
-            for (int h = 0; h < HALVES; ++h) {
-              tma_load_4d(kdst + h * kHalfBytes, &p.tmap_k, fb, h * 64, r.hkv, slot0, page, pol);
-              tma_load_4d(vdst + h * kHalfBytes, &p.tmap_v, fb, h * 64, r.hkv, slot0, page, pol);
+              for (int h = 0; h < HALVES; ++h) {
+                tma_load_4d(kdst + h * kHalfBytes, &p.tmap_k, fb, h * 64, cur.hkv, slot0, page, pol);
+                tma_load_4d(vdst + h * kHalfBytes, &p.tmap_v, fb, h * 64, cur.hkv, slot0, page, pol);
+              }
             }
+            __syncwarp();
+            ++kt;
+            if (++local == 2) do_next();
+            if (!ok) break;
           }
-          __syncwarp();
-          ++kt;
-        }
-      } else {
-        PlanSmall plan(r.a, r.e);
-        while (!plan.done()) {
-          const int st = kt % stages;
-          if (kt >= stages && lane == 0)
-            ok = mbar_wait(smem_u32(&bars[stages + st]), ((kt / stages) - 1) & 1, abort_flag);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          const Tile t = plan.next();
-          int nbox = 0;
-          int pages[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int k0 = t.jbase + 16 * c;
-            const bool need = (k0 <= t.khi) && (k0 + 15 >= t.klo);
-            pages[c] = need ? page_of(k0 / p.P) : 0;
-            nbox += need ? 1 : 0;
-          }
-          if (lane == 0) {
-            const uint32_t kdst = smem_u32(smem + st * STAGE_BYTES);
-            const uint32_t vdst = kdst + TILE_BYTES;
-            const uint32_t fb = smem_u32(&bars[st]);
-            mbar_arrive_expect_tx(fb, nbox * 2 * HALVES * 16 * 128);
+        } else {
+          PlanSmall plan(cur.a, cur.e);
+          while (!plan.done()) {
+            const int st = kt % stages;
+            if (kt >= stages && lane == 0)
+              ok = mbar_wait(smem_u32(&bars[stages + st]), ((kt / stages) - 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const Tile t = plan.next();
+            int nbox = 0;
+            int pages[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int k0 = t.jbase + 16 * c;
-              if (!((k0 <= t.khi) && (k0 + 15 >= t.klo))) continue;
-              if (pages[c] < 0 || pages[c] >= p.num_pages)
-                report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
-              const int slot = k0 % p.P;
+              const bool need = (k0 <= t.khi) && (k0 + 15 >= t.klo);
+              pages[c] = need ? page_of(k0 / p.P) : 0;
+              nbox += need ? 1 : 0;
+            }
+            if (lane == 0) {
+              const uint32_t kdst = smem_u32(smem + st * STAGE_BYTES);
+              const uint32_t vdst = kdst + TILE_BYTES;
+              const uint32_t fb = smem_u32(&bars[st]);
+              mbar_arrive_expect_tx(fb, nbox * 2 * HALVES * 16 * 128);
 #pragma unroll
-              for (int h = 0; h < HALVES; ++h) {
-                tma_load_4d(kdst + h * kHalfBytes + c * 16 * 128, &p.tmap_k, fb, h * 64, r.hkv,
-                            slot, pages[c], pol);
-                tma_load_4d(vdst + h * kHalfBytes + c * 16 * 128, &p.tmap_v, fb, h * 64, r.hkv,
-                            slot, pages[c], pol);
+              for (int c = 0; c < 4; ++c) {
+                const int k0 = t.jbase + 16 * c;
+                if (!((k0 <= t.khi) && (k0 + 15 >= t.klo))) continue;
+                if (pages[c] < 0 || pages[c] >= p.num_pages)
+                  report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+                const int slot = k0 % p.P;
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                  tma_load_4d(kdst + h * kHalfBytes + c * 16 * 128, &p.tmap_k, fb, h * 64, cur.hkv,
+                              slot, pages[c], pol);
+                  tma_load_4d(vdst + h * kHalfBytes + c * 16 * 128, &p.tmap_v, fb, h * 64, cur.hkv,
+                              slot, pages[c], pol);
+                }
               }
             }
+            __syncwarp();
+            ++kt;
+            if (++local == 2) do_next();
+            if (!ok) break;
           }
-          __syncwarp();
-          ++kt;
         }
       }
       if (!ok) break;
+      if (!nxt_done) do_next();
+      if (!ok) break;
+      cur = nxt;
+      cur_row = nxt_row;
+      cur_base = nxt_base;
+      cur_page = nxt_page;
     }
     if (!ok && lane == 0) {
       report(p.dev_err, INKLING_DEVERR_TIMEOUT);
-      // drain: wait for the copies already issued into stages nobody consumes
+      // drain: copies already issued into stages / slots nobody consumes
       for (int j = max(0, kt - stages); j < kt; ++j)
         mbar_wait_drain(smem_u32(&bars[j % stages]), (j / stages) & 1);
+      for (int j = max(0, ki - kItemSlots); j < ki; ++j)
+        mbar_wait_drain(smem_u32(&rfull[j % kItemSlots]), (j / kItemSlots) & 1);
     }
     return;
   }
@@ -331,18 +447,32 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   int kt = 0;
   bool ok = true;
   for (int ki = 0;; ++ki) {
-    // ---- next item
+    // ---- next item: record and q rows from the ring
     const int slot = ki % kItemSlots;
-    const bool got = mbar_wait_warp(smem_u32(&ifull[slot]), (ki / kItemSlots) & 1, abort_flag);
-    if (!got) {
+    if (!mbar_wait_warp(smem_u32(&rfull[slot]), (ki / kItemSlots) & 1, abort_flag)) {
       ok = false;
       break;
     }
-    const ItemRec r = ring[slot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&iempty[slot]));
-    if (r.b < 0) break;
+    const ItemRec r = *slot_rec(slot);
     const bool final_out = r.n_s <= 1;
+    uint32_t qf[KS][NT][2];
+    if (r.b >= 0 && r.nvis > 0) {
+      const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(slot_q(slot));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int head = nt * 8 + g;
+        const bool live = head < G;
+        const __nv_bfloat16* qrow = qs + (live ? head : 0) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qf[ks][nt][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4) : 0u;
+          qf[ks][nt][1] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8) : 0u;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));  // slot free: q is in registers
+    if (r.b < 0) break;
 
     if (r.nvis == 0) {  // empty sequence: out = 0, lse = -inf
       for (int i = tid; i < G * D; i += kConsumerThreads) {
@@ -354,35 +484,23 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       continue;
     }
 
-    // ---- per-item prologue: Q^T fragments and the bias slice
-    uint32_t qf[KS][NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int head = nt * 8 + g;
-      const bool live = head < G;
-      const __nv_bfloat16* qrow =
-          p.q + ((size_t)r.b * p.H_q + r.hkv * G + (live ? head : 0)) * D;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][nt][0] =
-            live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4)) : 0u;
-        qf[ks][nt][1] =
-            live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8)) : 0u;
-      }
-    }
-    const int dlo = min(r.pos - r.e, R - 1);
-    const int dhi = min(r.pos - r.a, R - 1);
-    const int cnt = dhi - dlo + 1;
-    const bool bias_in_smem = cnt <= p.nb;
     const float* rel_g = p.rel + ((size_t)r.b * p.H_q + r.hkv * G) * R;
-    named_bar_sync(1, kConsumerThreads);  // previous item's readers of bias_s / comb are done
-    if (bias_in_smem) {
-      for (int i = tid; i < G * cnt; i += kConsumerThreads) {
-        const int h = i / cnt, kk = i - h * cnt;
-        bias_s[h * p.nb + kk] = __ldg(rel_g + (size_t)h * R + dlo + kk) * kLog2e;
-      }
-    }
-    named_bar_sync(1, kConsumerThreads);
+    // bias of this thread's 4*NT scores of a tile (already in L2; loaded one
+    // tile ahead of its use)
+    auto load_bias = [&](const Tile& t, float (&bv)[NT][4]) {
+      const int key0 = t.jbase + r0;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int key = key0 + g + 8 * (i >> 1);
+          int h = nt * 8 + 2 * c4 + (i & 1);
+          h = h < G ? h : G - 1;
+          const bool v = key >= t.klo && key <= t.khi;
+          const int dcl = v ? min(r.pos - key, R - 1) : 0;
+          bv[nt][i] = __ldg(rel_g + (size_t)h * R + dcl);
+        }
+    };
 
     float m_run[NT][2], l_run[NT][2];
     float o_acc[KS][NT][4];
@@ -396,7 +514,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         for (int i = 0; i < 4; ++i) o_acc[mt][nt][i] = 0.f;
     }
 
-    auto tile_body = [&](const Tile& t, int st) {
+    auto tile_body = [&](const Tile& t, int st, const float (&bv)[NT][4]) {
       const int key0 = t.jbase + r0;  // key of this warp's first row
       if (!(key0 <= t.khi && key0 + 15 >= t.klo)) return;
       const bool part = (key0 < t.klo) || (key0 + 15 > t.khi);
@@ -432,16 +550,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int kr = i >> 1;
-          int h = nt * 8 + 2 * c4 + (i & 1);
-          h = h < G ? h : G - 1;
-          const int dcl = min(r.pos - (key0 + g + 8 * kr), R - 1);
-          float bias;
-          if (bias_in_smem) {
-            bias = bias_s[h * p.nb + (vk[kr] ? dcl - dlo : 0)];
-          } else {
-            bias = vk[kr] ? __ldg(rel_g + (size_t)h * R + dcl) * kLog2e : 0.f;
-          }
-          const float s = fmaf(sacc[nt][i], sl2, bias);
+          const float s = fmaf(sacc[nt][i], sl2, bv[nt][i] * kLog2e);
           sacc[nt][i] = vk[kr] ? s : -INFINITY;
         }
       }
@@ -508,34 +617,42 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       }
     };
 
-    // ---- tile loop (same walk as the producer)
-    auto consume = [&](const Tile& t) -> bool {
-      const int st = kt % stages;
-      if (!mbar_wait_warp(smem_u32(&bars[st]), (kt / stages) & 1, abort_flag)) return false;
-      tile_body(t, st);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars[stages + st]));
-      ++kt;
-      return true;
+    // ---- tile loop (same walk as the producer), bias loaded one tile ahead
+    auto run_tiles = [&](auto& plan, auto next_fn) -> bool {
+      Tile t = next_fn(plan);
+      float bv[NT][4];
+      load_bias(t, bv);
+      while (true) {
+        const int st = kt % stages;
+        if (!mbar_wait_warp(smem_u32(&bars[st]), (kt / stages) & 1, abort_flag)) return false;
+        const bool more = !plan.done();
+        Tile tn = t;
+        float bn[NT][4];
+        if (more) {
+          tn = next_fn(plan);
+          load_bias(tn, bn);
+        }
+        tile_body(t, st, bv);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars[stages + st]));
+        ++kt;
+        if (!more) return true;
+        t = tn;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) bv[nt][i] = bn[nt][i];
+      }
     };
     if constexpr (BH == 64) {
       PlanBig plan(r.a, r.e, p.P);
-      while (!plan.done()) {
+      ok = run_tiles(plan, [](PlanBig& pl) {
         int lp, s0;
-        const Tile t = plan.next(lp, s0);
-        if (!consume(t)) {
-          ok = false;
-          break;
-        }
-      }
+        return pl.next(lp, s0);
+      });
     } else {
       PlanSmall plan(r.a, r.e);
-      while (!plan.done()) {
-        if (!consume(plan.next())) {
-          ok = false;
-          break;
-        }
-      }
+      ok = run_tiles(plan, [](PlanSmall& pl) { return pl.next(); });
     }
     if (!ok) break;
 
@@ -551,6 +668,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         l_run[nt][j] = v;
       }
     constexpr int OP = D + 4;
+    named_bar_sync(1, kConsumerThreads);  // previous item's readers of comb_* are done
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
@@ -597,7 +715,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         if (d == 0) p.lse_part[row * S + r.split] = lse;
       }
     }
-    // the next item's first named barrier orders these reads before reuse
   }
   if (!ok && lane == 0) report(p.dev_err, INKLING_DEVERR_TIMEOUT);
 }
@@ -723,28 +840,25 @@ int launch_decode(const DecodeCall& c) {
   prm.S = c.S;
   prm.chunk = c.chunk;
   prm.scale_log2 = c.scale * kLog2e;
-  prm.total_items = c.B * c.H_kv * c.S;
-
-  // bias entries per head: the widest distance range one item can need
-  const int keys_item = (c.S > 1) ? c.chunk : c.keys_max;
-  int nb = std::max(1, std::min(c.R, keys_item));
+  prm.bias_prefetch = (c.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(c.rel) & 15) == 0);
+  const int n_prefix = c.S > 1 ? c.B + 1 : 0;
   // kCtasPerSm CTAs per SM: keep each CTA under the budget; 2..max stages
   const int budget = INKLING_DECODE_SMEM_BUDGET_KB * 1024;
   int stages = INKLING_DECODE_MAX_STAGES;
-  while (stages > 2 && DecodeSmem(c.D, G, NT, nb, stages).total > budget) --stages;
-  if (DecodeSmem(c.D, G, NT, nb, stages).total > budget) nb = 1;  // bias read through L1/L2
-  prm.nb = nb;
+  while (stages > 2 && DecodeSmem(c.D, G, NT, stages, n_prefix).total > budget) --stages;
   prm.stages = stages;
-  const int smem = 1024 + DecodeSmem(c.D, G, NT, nb, stages).total;
+  const int smem = 1024 + DecodeSmem(c.D, G, NT, stages, n_prefix).total;
+  if (smem > 227 * 1024) return INKLING_ERR_ARG;  // batch too large for the item prefix table
 
-  // Static schedule: give every CTA the same number of items (a grid of
-  // ceil(items / waves) CTAs), so the last wave is not a partial one.
-  // Dynamic schedule (splits of uneven length): fill every slot.
+  // Static schedule (one split per sequence): give every CTA the same number
+  // of items (a grid of ceil(items / waves) CTAs), so the last wave is not a
+  // partial one.  Dynamic schedule (splits): fill every slot.
+  const int total_items = c.B * c.H_kv * c.S;
   const int slots = kCtasPerSm * sm_count();
-  int grid = std::min(prm.total_items, slots);
+  int grid = std::min(total_items, slots);
   if (!c.counter && INKLING_DECODE_BALANCED) {
-    const int waves = (prm.total_items + slots - 1) / slots;
-    grid = (prm.total_items + waves - 1) / waves;
+    const int waves = (total_items + slots - 1) / slots;
+    grid = (total_items + waves - 1) / waves;
   }
   grid = std::max(1, grid);
   if (c.counter && cudaMemsetAsync(c.counter, 0, sizeof(int32_t), c.stream) != cudaSuccess)
