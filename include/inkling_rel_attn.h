@@ -110,6 +110,34 @@ int inkling_rel_attn_decode(
     void* stream);
 
 /*
+ * inkling_rel_attn_decode_noalloc -- inkling_rel_attn_decode without a
+ * caller-provided workspace, for callers that cannot allocate device memory
+ * (for example a plugin inside a host framework that owns all device memory
+ * and forbids allocation during a step, or a binding with no access to the
+ * CUDA allocator).  The pages describe no such entry point; it has no
+ * counterpart there.
+ *
+ * Same arguments and result as inkling_rel_attn_decode minus workspace /
+ * workspace_bytes.  Split partials live in a fixed 32 MiB device array inside
+ * the library (one per GPU that loads it, held until process exit).  A call
+ * needing more scratch than that (see
+ * inkling_rel_attn_decode_workspace_size) returns INKLING_ERR_WORKSPACE and
+ * launches nothing.  Nothing is allocated.  All calls on a device share the
+ * array: calls whose kernels may overlap on the GPU race and must be ordered
+ * by the caller.  The first call on each device resolves the array's device
+ * address (cudaGetSymbolAddress) with that device current; make it outside any
+ * stream capture.
+ */
+int inkling_rel_attn_decode_noalloc(
+    const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* page_table, int32_t page_table_stride,
+    const int32_t* seq_lens, const float* rel_logits,
+    int32_t B, int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size,
+    int32_t num_pages, int32_t R, int32_t window, float scale,
+    int32_t max_seq_len, void* out, float* lse_out, int32_t num_splits,
+    int32_t* device_error, void* stream);
+
+/*
  * inkling_rel_attn_prefill -- chunked / paged prefill (TensorRT-LLM PR #17062,
  * "Implementation": paged prefill over the cache).
  *

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libinkling_rel_attn.so")
 #: C entry points (the names declared in include/inkling_rel_attn.h)
 EXPORTED = (
     "inkling_rel_attn_decode",
+    "inkling_rel_attn_decode_noalloc",
     "inkling_rel_attn_prefill",
     "inkling_rel_attn_choose_splits",
     "inkling_rel_attn_decode_workspace_size",
@@ -38,6 +39,11 @@ _SIGS = {
         _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B H_q H_kv D page_size num_pages R
         _i32, _f32, _i32,                           # window scale max_seq_len
         _p, _p, _p, _sz, _i32, _p, _p]),            # out lse ws ws_bytes splits err stream
+    "inkling_rel_attn_decode_noalloc": (ctypes.c_int, [
+        _p, _p, _p, _p, _i32, _p, _p,               # q k v page_table stride seq_lens rel
+        _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B H_q H_kv D page_size num_pages R
+        _i32, _f32, _i32,                           # window scale max_seq_len
+        _p, _p, _i32, _p, _p]),                     # out lse splits err stream
     "inkling_rel_attn_prefill": (ctypes.c_int, [
         _p, _p, _p, _p, _p, _i32, _p, _p,           # q cu k v page_table stride seq_lens rel
         _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B T max_q_len H_q H_kv D page_size
@@ -81,6 +87,18 @@ def inkling_rel_attn_decode(q, k_cache, v_cache, page_table, page_table_stride, 
         _v(rel_logits), B, H_q, H_kv, D, page_size, num_pages, R, window, scale, max_seq_len,
         _v(out), _v(lse_out), _v(workspace), workspace_bytes, num_splits, _v(device_error),
         _v(stream))
+
+
+def inkling_rel_attn_decode_noalloc(q, k_cache, v_cache, page_table, page_table_stride, seq_lens,
+                                    rel_logits, B, H_q, H_kv, D, page_size, num_pages, R, window,
+                                    scale, max_seq_len, out, lse_out, num_splits, device_error,
+                                    stream):
+    """inkling_rel_attn_decode with the library's fixed scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    return load().inkling_rel_attn_decode_noalloc(
+        _v(q), _v(k_cache), _v(v_cache), _v(page_table), page_table_stride, _v(seq_lens),
+        _v(rel_logits), B, H_q, H_kv, D, page_size, num_pages, R, window, scale, max_seq_len,
+        _v(out), _v(lse_out), num_splits, _v(device_error), _v(stream))
 
 
 def inkling_rel_attn_prefill(q, cu_seqlens_q, k_cache, v_cache, page_table, page_table_stride,
