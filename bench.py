@@ -160,46 +160,15 @@ def decode_bytes(inp):
 # ---------------------------------------------------------------------------
 # our arm
 
-def bench_decode(args, device, rank):
-    import paged_attention_relative_attn_gb300 as ira
-    name = args.workload
-    sets = []
-    n_sets = 0
-    kv_bytes = total_bytes = None
-    while True:
-        inp = W.make_decode_config(name, device=device, seed=n_sets, batch=args.batch)
-        kvb, totb = decode_bytes(inp)
-        sets.append(inp)
-        n_sets += 1
-        kv_bytes = kvb if kv_bytes is None else kv_bytes
-        if args.sets is not None:
-            if n_sets >= args.sets:
-                break
-        # rotate until the distinct visible K/V of one rotation exceeds 2x L2
-        elif n_sets >= 3 and sum(decode_bytes(s)[0] for s in sets) > 2 * L2_BYTES:
-            break
-    per_set = [decode_bytes(s) for s in sets]
-    B, H_q, H_kv, D = sets[0].B, sets[0].H_q, sets[0].H_kv, sets[0].D
-    S = ira.choose_splits(B, H_kv, sets[0].window, sets[0].max_seq_len,
-                          torch.cuda.get_device_properties(device).multi_processor_count)
-    ws_bytes = ira.decode_workspace_bytes(B, H_q, H_kv, D, sets[0].window, sets[0].max_seq_len)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
-    outs = [torch.empty_like(s.q) for s in sets]
-    lses = [torch.empty((B, H_q), dtype=torch.float32, device=device) for s in sets]
-
-    def step(i, stream=None):
-        s = sets[i % n_sets]
-        ira.decode_inputs(s, out=outs[i % n_sets], lse=lses[i % n_sets], workspace=ws,
-                          stream=stream)
-
-    # warm-up (eager)
-    for i in range(max(args.warmup, 3)):
-        step(i)
+def time_steps(args, device, step, K, warmup, per_graph):
+    """Warm up eagerly, capture `per_graph` consecutive steps in a CUDA graph,
+    then time exactly K steps (graph replays + a remainder graph) with events
+    on the capture stream while nvidia-smi samples the clocks.  Returns
+    (ms for the K steps, clock summary)."""
+    for i in range(max(warmup, 3)):
+        step(i, None)
     torch.cuda.synchronize()
-
-    K = args.steps
-    g_len = min(K, 60 * n_sets // math.gcd(60, n_sets))  # whole rotations per graph
-    g_len = max(1, min(g_len, K))
+    g_len = max(1, min(K, per_graph))
     cap = torch.cuda.Stream(device)
     cap.wait_stream(torch.cuda.current_stream())
 
@@ -208,7 +177,7 @@ def bench_decode(args, device, rank):
         with torch.cuda.stream(cap):
             with torch.cuda.graph(g, stream=cap):
                 for i in range(n):
-                    step(i, stream=cap)
+                    step(i, cap)
         return g
 
     g_main = make_graph(g_len)
@@ -217,7 +186,6 @@ def bench_decode(args, device, rank):
     torch.cuda.synchronize()
     g_main.replay()  # one more warm-up pass through the graph
     torch.cuda.synchronize()
-
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     barrier(args)
@@ -232,19 +200,139 @@ def bench_decode(args, device, rank):
             ev1.record(cap)
         torch.cuda.synchronize()
     barrier(args)
-    ms = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(args, ms)
+    ms = max_over_ranks(args, ev0.elapsed_time(ev1))
+    return ms, clk.summary()
 
-    # bytes of exactly the K steps that ran (rotation order i % n_sets)
+
+def bench_decode(args, device, name, K, warmup):
+    import paged_attention_relative_attn_gb300 as ira
+    sets = []
+    while True:
+        sets.append(W.make_decode_config(name, device=device, seed=len(sets), batch=args.batch))
+        if args.sets is not None:
+            if len(sets) >= args.sets:
+                break
+        # rotate until the distinct visible K/V of one rotation exceeds 2x L2
+        elif len(sets) >= 3 and sum(decode_bytes(x)[0] for x in sets) > 2 * L2_BYTES:
+            break
+    n_sets = len(sets)
+    per_set = [decode_bytes(x) for x in sets]
+    B, H_q, H_kv, D = sets[0].B, sets[0].H_q, sets[0].H_kv, sets[0].D
+    S = ira.choose_splits(B, H_kv, sets[0].window, sets[0].max_seq_len,
+                          torch.cuda.get_device_properties(device).multi_processor_count)
+    ws_bytes = ira.decode_workspace_bytes(B, H_q, H_kv, D, sets[0].window, sets[0].max_seq_len)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    outs = [torch.empty_like(x.q) for x in sets]
+    lses = [torch.empty((B, H_q), dtype=torch.float32, device=device) for x in sets]
+
+    def step(i, stream):
+        x = sets[i % n_sets]
+        ira.decode_inputs(x, out=outs[i % n_sets], lse=lses[i % n_sets], workspace=ws,
+                          stream=stream)
+
+    ms, clocks = time_steps(args, device, step, K, warmup, 60 * n_sets // math.gcd(60, n_sets))
     kv_total = sum(per_set[i % n_sets][0] for i in range(K))
     all_total = sum(per_set[i % n_sets][1] for i in range(K))
-    launches_per_step = 1 + (1 if S > 1 else 0)
+    launches = K * (1 + (1 if S > 1 else 0))
+    x0 = sets[0]
+    config = {"workload": name, "batch": B, "heads": f"{H_q}/{H_kv}", "head_dim": D,
+              "page_size": x0.page_size, "window": x0.window, "R": x0.R, "num_splits": S,
+              "l2": f"rotating {n_sets} input sets, {sum(p[0] for p in per_set) / 1e6:.0f} MB of "
+                    f"visible K/V per rotation (L2 129 MB)"}
+    return dict(ms=ms, K=K, clocks=clocks, launches=launches, config=config, sets=sets, ws=ws,
+                units_total=kv_total, bytes_total=all_total, kernel="decode_kernel",
+                kernel_launches=K, unit="GB/s")
 
-    res = dict(ms=ms, kv_total=kv_total, all_total=all_total, K=K, S=S, n_sets=n_sets,
-               launches=K * launches_per_step, clocks=clk.summary(), sets=sets, outs=outs,
-               lses=lses, ws=ws, kv_per_step=sum(p[0] for p in per_set) / n_sets,
-               total_per_step=sum(p[1] for p in per_set) / n_sets)
-    return res
+
+def prefill_work(inp, window):
+    """Algorithmic work of one prefill call: MMA flops over visible (query,
+    key) pairs and bytes (visible bias entries, q, out, K/V of the key range)."""
+    cu = inp.cu_seqlens_q.cpu().tolist()
+    sl = inp.seq_lens.cpu().tolist()
+    pairs = 0
+    kv_keys = 0
+    for b in range(inp.B):
+        n = cu[b + 1] - cu[b]
+        L = sl[b]
+        if n == 0:
+            continue
+        pos = torch.arange(L - n, L, dtype=torch.int64)
+        vis = torch.clamp(pos + 1, max=window) if window > 0 else pos + 1
+        pairs += int(vis.sum())
+        lo = max(0, L - n - window + 1) if window > 0 else 0
+        kv_keys += L - lo
+    flops = 4 * inp.D * pairs * inp.H_q
+    bias = pairs * inp.H_q * 4
+    qo = inp.T * inp.H_q * inp.D * 2 * 2
+    kv = kv_keys * inp.H_kv * inp.D * 2 * 2
+    return flops, bias + qo + kv + inp.T * inp.H_q * 4
+
+
+def bench_prefill(args, device, K, warmup):
+    """One step = the whole chunked prefill: 4 calls, each 4 sequences x 2048
+    new tokens against the cached prefix (positions 2048c .. 2048c+2047)."""
+    import paged_attention_relative_attn_gb300 as ira
+    chunks = []
+    cache = None
+    for c in range(4):
+        inp, cache = W.make_chunked_prefill(c, device=device, seed=0, cache=cache)
+        chunks.append(inp)
+    work = [prefill_work(x, x.window) for x in chunks]
+    outs = [torch.empty_like(x.q) for x in chunks]
+    lses = [torch.empty(x.q.shape[:2], dtype=torch.float32, device=device) for x in chunks]
+
+    def step(i, stream):
+        for c, x in enumerate(chunks):
+            ira.prefill_inputs(x, out=outs[c], lse=lses[c], stream=stream)
+
+    ms, clocks = time_steps(args, device, step, K, warmup, 10)
+    flops = K * sum(w[0] for w in work)
+    nbytes = K * sum(w[1] for w in work)
+    x0 = chunks[0]
+    config = {"workload": "chunked_prefill", "sequences": 4, "seq_len": 8192, "chunk": 2048,
+              "tokens_per_call": x0.T, "heads": f"{x0.H_q}/{x0.H_kv}", "head_dim": x0.D,
+              "window": x0.window, "R": x0.R, "page_size": x0.page_size,
+              "l2": "805 MB of rel_logits per call (L2 129 MB)"}
+    return dict(ms=ms, K=K, clocks=clocks, launches=4 * K, config=config, units_total=flops,
+                bytes_total=nbytes, kernel="prefill_kernel", kernel_launches=4 * K, unit="TFLOP/s")
+
+
+def bench_stack(args, device, K, warmup):
+    """One step = one decode step over the 66-layer stack: 55 local layers
+    (16 KV heads, window 512, R=512) and 11 global layers (8 KV heads, full
+    causal, R=1024), batch 128 with lognormal lengths, fresh K/V/bias per
+    layer (every layer's own paged pool)."""
+    import paged_attention_relative_attn_gb300 as ira
+    s = W.STACK
+    lens = W.draw_stack_lengths(0)
+    layers = []
+    for layer in range(s["n_layers"]):
+        c = s["glob"] if W.is_global_layer(layer) else s["local"]
+        layers.append(W.make_decode(s["B"], s["H_q"], c["H_kv"], s["D"], s["P"], lens,
+                                    c["window"], c["R"], device=device, seed=1000 + layer,
+                                    max_seq_len=s["max_len"]))
+    ws_bytes = max(ira.decode_workspace_bytes(x.B, x.H_q, x.H_kv, x.D, x.window, x.max_seq_len)
+                   for x in layers)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(layers[0].q)
+    lse = torch.empty(layers[0].q.shape[:2], dtype=torch.float32, device=device)
+    per_layer = [decode_bytes(x) for x in layers]
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    n_merge = sum(1 for x in layers if ira.choose_splits(x.B, x.H_kv, x.window, x.max_seq_len, sms) > 1)
+
+    def step(i, stream):
+        for x in layers:
+            ira.decode_inputs(x, out=out, lse=lse, workspace=ws, stream=stream)
+
+    ms, clocks = time_steps(args, device, step, K, warmup, 4)
+    config = {"workload": "decode_66_layers", "layers": "55 local (48/16, W=512, R=512) + 11 "
+              "global (48/8, causal, R=1024)", "batch": s["B"], "head_dim": s["D"],
+              "page_size": s["P"], "lengths": "lognormal mean 2048, sigma 0.5, clipped [1, 8192]",
+              "l2": f"{sum(p[0] for p in per_layer) / 1e9:.1f} GB of visible K/V per step"}
+    return dict(ms=ms, K=K, clocks=clocks, launches=K * (len(layers) + n_merge), config=config,
+                units_total=K * sum(p[0] for p in per_layer),
+                bytes_total=K * sum(p[1] for p in per_layer), kernel="decode_kernel",
+                kernel_launches=K * len(layers), unit="GB/s")
 
 
 def bench_decode_e2e(args, device, sets, ws):
@@ -403,14 +491,68 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+DEFAULT_STEPS = {"local_decode": 10000, "global_decode": 2000, "chunked_prefill": 200,
+                 "decode_66_layers": 40}
+KERNEL_SOURCES = {
+    "decode_kernel": ["paged_attention_relative_attn_gb300/csrc/decode.cu",
+                      "paged_attention_relative_attn_gb300/csrc/plan.cuh",
+                      "paged_attention_relative_attn_gb300/csrc/ptx.cuh"],
+    "prefill_kernel": ["paged_attention_relative_attn_gb300/csrc/prefill.cu",
+                       "paged_attention_relative_attn_gb300/csrc/plan.cuh",
+                       "paged_attention_relative_attn_gb300/csrc/ptx.cuh",
+                       "paged_attention_relative_attn_gb300/csrc/tc.cuh"],
+}
+
+
+def run_workload(args, device, name, K, warmup):
+    if name in ("local_decode", "global_decode"):
+        return bench_decode(args, device, name, K, warmup)
+    if name == "chunked_prefill":
+        return bench_prefill(args, device, K, warmup)
+    return bench_stack(args, device, K, warmup)
+
+
+def summarize(args, r, pk):
+    """Metric value, roofline and the common keys of one workload's result."""
+    ms = r["ms"]
+    sec = ms * 1e-3
+    units = sum_over_ranks(args, r["units_total"])
+    nbytes = sum_over_ranks(args, r["bytes_total"])
+    per_launch_s = sec / r["kernel_launches"]
+    bytes_per_launch = r["bytes_total"] / r["kernel_launches"]
+    achieved = bytes_per_launch / per_launch_s / 1e9
+    name = r["config"]["workload"]
+    roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"],
+            "traffic": traffic_record(r["kernel"], name, KERNEL_SOURCES[r["kernel"]]),
+            "kernel": r["kernel"], "peak_source": f"{pk['source']} hbm_gbs (of {pk['source']})",
+            "bytes_per_launch": bytes_per_launch}
+    out = {"value": None, "unit": r["unit"], "ms_per_step": ms / r["K"], "steps": r["K"],
+           "config": r["config"], "clocks": r["clocks"], "gpu_launches": r["launches"]}
+    if r["unit"] == "TFLOP/s":
+        tflops = units / sec / 1e12
+        out["value"] = tflops
+        roof["tflops"] = tflops / args.world
+        roof["tensor_peak_tflops"] = pk["bf16_tflops"]
+        roof["tensor_frac"] = tflops / args.world / pk["bf16_tflops"]
+        out["metric"] = METRIC + " [prefill TFLOP/s]"
+    else:
+        out["value"] = units / sec / 1e9
+        roof["kv_frac"] = units / args.world / sec / 1e9 / pk["hbm_gbs"]
+        out["metric"] = METRIC
+    out["roofline"] = roof
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="local_decode",
-                    choices=["local_decode", "global_decode"])
+                    choices=["local_decode", "global_decode", "chunked_prefill",
+                             "decode_66_layers"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=5.0)
@@ -418,8 +560,14 @@ def main():
                     help="keep only the first sequences (profiling of a smaller case)")
     ap.add_argument("--sets", type=int, default=None, help="number of rotated input sets")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the secondary workloads (global decode, prefill, 66-layer step)")
     args = ap.parse_args()
     args.world, args.rank, args.local = dist_env()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+    if args.workload not in ("local_decode", "global_decode") and args.impl == "reference":
+        args.workload = "local_decode"
 
     if args.impl == "reference":
         run_reference(args)
@@ -435,48 +583,40 @@ def main():
     _lib.load()
 
     pk = peaks()
-    r = bench_decode(args, device, args.rank)
-    if args.no_e2e:
-        e2e = None
-    else:
+    r = run_workload(args, device, args.workload, args.steps, args.warmup)
+    head = summarize(args, r, pk)
+    line = {"metric": head["metric"], "value": head["value"], "unit": head["unit"],
+            "n_gpus": args.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(head["config"], parallelism=f"replicas x{args.world}",
+                           timing="CUDA graph replay of exactly K steps, CUDA events"),
+            "clocks": head["clocks"], "gpu_launches": head["gpu_launches"],
+            "roofline": head["roofline"]}
+    if args.workload in ("local_decode", "global_decode") and not args.no_e2e:
         e2e = bench_decode_e2e(args, device, r["sets"], r["ws"])
         e2e["value"] = sum_over_ranks(args, e2e["value"])
-    ms = r["ms"]
-    kv_total = sum_over_ranks(args, r["kv_total"])
-    value = kv_total / (ms * 1e-3) / 1e9
-    # dominant kernel: the decode kernel (one launch per step when S == 1)
-    per_launch_ms = ms / r["K"]
-    achieved = r["total_per_step"] / (per_launch_ms * 1e-3) / 1e9
-    traffic = traffic_record("decode_kernel", args.workload,
-                             ["paged_attention_relative_attn_gb300/csrc/decode.cu",
-                              "paged_attention_relative_attn_gb300/csrc/ptx.cuh"])
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": args.workload, "batch": r["sets"][0].B,
-                   "heads": f"{r['sets'][0].H_q}/{r['sets'][0].H_kv}", "head_dim": r["sets"][0].D,
-                   "page_size": r["sets"][0].page_size, "window": r["sets"][0].window,
-                   "R": r["sets"][0].R, "num_splits": r["S"],
-                   "l2": f"rotating {r['n_sets']} input sets, {r['kv_per_step'] * r['n_sets'] / 1e6:.0f} MB "
-                         f"of visible K/V per rotation (L2 129 MB)",
-                   "parallelism": f"replicas x{args.world}", "timing": "CUDA graph replay, events"},
-        "clocks": r["clocks"],
-        "e2e": e2e,
-        "gpu_launches": r["launches"],
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "peak_source": f"{pk['source']} hbm_gbs",
-                     "kv_frac": value / args.world / pk["hbm_gbs"]},
-    }
-    if args.rank == 0 and not args.no_cpu_baseline:
+        line["e2e"] = e2e
+    else:
+        line["e2e"] = None
+    if args.rank == 0 and not args.no_cpu_baseline and "sets" in r:
         gbs, n, t = oracle_units(r["sets"][0], args.cpu_budget)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": blas_threads(),
                                 "kind": "oracle",
                                 "sample": f"{n} (sequence, KV head) units of {args.workload} "
                                           f"(first of {r['sets'][0].B * r['sets'][0].H_kv}), "
                                           f"{t:.1f} s of fp64 oracle time"}
+    del r
+    torch.cuda.empty_cache()
+    if not args.no_extra and args.workload == "local_decode":
+        extra = {}
+        for name, K in (("global_decode", 1000), ("chunked_prefill", 100),
+                        ("decode_66_layers", 20)):
+            rr = run_workload(args, device, name, K, 5)
+            extra[name] = summarize(args, rr, pk)
+            del rr
+            torch.cuda.empty_cache()
+        line["extra_workloads"] = extra
     if args.rank == 0:
         print(json.dumps(line), flush=True)
     if args.world > 1:

@@ -44,9 +44,10 @@
 
 namespace ira {
 
-constexpr int kPrefThreads = 192;
+constexpr int kPrefThreads = 256;
 constexpr int kQRows = 128;
-constexpr int kKvStages = 2;
+constexpr int kKStages = 3;  // K tiles: released when QK^T has read them
+constexpr int kVStages = 2;  // V tiles: released when PV has read them
 constexpr int kBiasBufs = 3;
 constexpr int kBiasPitch = 68;                       // floats per row band (64 + alignment)
 constexpr int kBiasWarpBytes = 32 * kBiasPitch * 4;  // 32 rows of one warp
@@ -66,6 +67,7 @@ struct PrefillParams {
   int32_t* dev_err;
   int B, T, H_q, H_kv, G, P, num_pages, R, window, pt_stride, tiles_per_seq, max_q_len;
   float scale_log2;
+  float scale;
 };
 
 template <int D>
@@ -74,21 +76,22 @@ struct PrefillSmem {
   static constexpr int QHALF = kQRows * 128;
   static constexpr int Q_BYTES = HALVES * QHALF;
   static constexpr int TILE_BYTES = HALVES * kHalfBytes;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int KV_OFF = Q_BYTES;
-  static constexpr int BIAS_OFF = KV_OFF + kKvStages * STAGE_BYTES;
+  static constexpr int K_OFF = Q_BYTES;
+  static constexpr int V_OFF = K_OFF + kKStages * TILE_BYTES;
+  static constexpr int BIAS_OFF = V_OFF + kVStages * TILE_BYTES;
   static constexpr int BAR_OFF = BIAS_OFF + kBiasBufs * kBiasBufBytes;
-  // q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done
-  static constexpr int NBARS = 1 + 2 * kKvStages + 2 + 2 + 1;
+  // q_full, k_full/empty, v_full/empty, s_full[2], p_full[2], pv_done, b_full/empty
+  static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 2 * kBiasBufs;
   static constexpr int TOTAL = BAR_OFF + NBARS * 8 + 16;
 };
 
-// Bias + scale + mask of one 64-key tile for one query row.  OFF is the
+// Scale + bias + mask of one 64-key tile for one query row, in natural-log
+// units (s = scale * <q, k> + bias).  OFF is the
 // warp-uniform alignment of the row's band in shared memory: the bias of key
 // column c sits at float OFF + 63 - c of the band.
 template <int OFF>
 __device__ __forceinline__ void score_tile(float (&s)[64], const uint32_t (&sraw)[2][32],
-                                           const float* band, float sl2, int cl, int ch,
+                                           const float* band, float scale, int cl, int ch,
                                            bool full_vis, bool clamp, int dtop, int Rm1,
                                            float clampv) {
 #pragma unroll
@@ -107,9 +110,9 @@ __device__ __forceinline__ void score_tile(float (&s)[64], const uint32_t (&sraw
     for (int cc = 0; cc < 32; ++cc) {
       const int c = 32 * hh + cc;
       const int idx = OFF + 63 - c - (hh == 0 ? 32 : 0);
-      float bv = bb[idx] * kLog2e;
+      float bv = bb[idx];
       if (clamp) bv = (dtop - c >= Rm1) ? clampv : bv;
-      float v = fmaf(__uint_as_float(sraw[hh][cc]), sl2, bv);
+      float v = fmaf(__uint_as_float(sraw[hh][cc]), scale, bv);
       if (!full_vis) v = (c >= cl && c <= ch) ? v : -INFINITY;
       s[c] = v;
     }
@@ -163,25 +166,37 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + kKvStages;
-  uint64_t* s_full = kv_empty + kKvStages;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + kKStages;
+  uint64_t* v_full = k_empty + kKStages;
+  uint64_t* v_empty = v_full + kVStages;
+  uint64_t* s_full = v_empty + kVStages;
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_done + 1);
+  uint64_t* b_full = pv_done + 1;
+  uint64_t* b_empty = b_full + kBiasBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_empty + kBiasBufs);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (tid == 0) {
     mbar_init(smem_u32(q_full), 1);
-    for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(smem_u32(&kv_full[s]), 1);
-      mbar_init(smem_u32(&kv_empty[s]), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&p_full[s]), 4);
     }
     mbar_init(smem_u32(pv_done), 1);
+    for (int s = 0; s < kBiasBufs; ++s) {
+      mbar_init(smem_u32(&b_full[s]), 1);   // the bias loader warp
+      mbar_init(smem_u32(&b_empty[s]), 4);  // the four softmax warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -194,25 +209,36 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // =================================================================== loader
-  if (warp == 0) {
+  // =================================================================== loaders
+  if (warp == 0 || warp == 6) {
+    // warp 0: the Q tile, then K tiles into a kKStages ring; warp 6: V tiles
+    // into a kVStages ring.  Both walk the same page-respecting tile plan.
+    const bool is_k = warp == 0;
     if (lane == 0) {
-      for (int r = 0; r < 4; ++r) tmap_prefetch(&p.tmap_q[r]);
-      tmap_prefetch(&p.tmap_k);
-      tmap_prefetch(&p.tmap_v);
-      // Q tile: row group j (rows j + 4y) = tokens t0 + j + 4y
-      int ngroups = 0;
-      for (int j = 0; j < 4; ++j) ngroups += (j < nrows) ? 1 : 0;
-      const uint64_t pol_q = policy_evict_first();
-      mbar_arrive_expect_tx(smem_u32(q_full), ngroups * HALVES * 32 * 128);
-      for (int j = 0; j < 4; ++j) {
-        if (j >= nrows) continue;
-        const int tok = t0 + j;
-        for (int hh = 0; hh < HALVES; ++hh)
-          tma_load_3d(smem_u32(smem + hh * SM::QHALF + 32 * j * 128), &p.tmap_q[tok & 3],
-                      smem_u32(q_full), hh * 64, h, tok >> 2, pol_q);
+      if (is_k) {
+        for (int r = 0; r < 4; ++r) tmap_prefetch(&p.tmap_q[r]);
+        tmap_prefetch(&p.tmap_k);
+        // Q tile: row group j (rows j + 4y) = tokens t0 + j + 4y
+        int ngroups = 0;
+        for (int j = 0; j < 4; ++j) ngroups += (j < nrows) ? 1 : 0;
+        const uint64_t pol_q = policy_evict_first();
+        mbar_arrive_expect_tx(smem_u32(q_full), ngroups * HALVES * 32 * 128);
+        for (int j = 0; j < 4; ++j) {
+          if (j >= nrows) continue;
+          const int tok = t0 + j;
+          for (int hh = 0; hh < HALVES; ++hh)
+            tma_load_3d(smem_u32(smem + hh * SM::QHALF + 32 * j * 128), &p.tmap_q[tok & 3],
+                        smem_u32(q_full), hh * 64, h, tok >> 2, pol_q);
+        }
+      } else {
+        tmap_prefetch(&p.tmap_v);
       }
     }
+    const CUtensorMap* tmap = is_k ? &p.tmap_k : &p.tmap_v;
+    const int nst = is_k ? kKStages : kVStages;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    uint8_t* ring = smem + (is_k ? SM::K_OFF : SM::V_OFF);
     const uint64_t pol_kv = policy_evict_last();
     const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride;
     int batch_base = -1000000;
@@ -230,24 +256,21 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     if constexpr (BH == 64) {
       PlanBig plan(klo_all, khi_all, p.P);
       while (!plan.done()) {
-        const int st = kt % kKvStages;
-        if (kt >= kKvStages && lane == 0)
-          ok = mbar_wait(smem_u32(&kv_empty[st]), ((kt / kKvStages) - 1) & 1, abort_flag);
+        const int st = kt % nst;
+        if (kt >= nst && lane == 0)
+          ok = mbar_wait(smem_u32(&empty[st]), ((kt / nst) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         int lp, slot0;
         plan.next(lp, slot0);
         const int page = page_of(lp);
         if (lane == 0) {
-          if (page < 0 || page >= p.num_pages) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
-          const uint32_t kdst = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES);
-          const uint32_t vdst = kdst + TILE_BYTES;
-          const uint32_t fb = smem_u32(&kv_full[st]);
-          mbar_arrive_expect_tx(fb, 2 * TILE_BYTES);
-          for (int hh = 0; hh < HALVES; ++hh) {
-            tma_load_4d(kdst + hh * kHalfBytes, &p.tmap_k, fb, hh * 64, hkv, slot0, page, pol_kv);
-            tma_load_4d(vdst + hh * kHalfBytes, &p.tmap_v, fb, hh * 64, hkv, slot0, page, pol_kv);
-          }
+          if (is_k && (page < 0 || page >= p.num_pages)) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+          const uint32_t dst = smem_u32(ring + st * TILE_BYTES);
+          const uint32_t fb = smem_u32(&full[st]);
+          mbar_arrive_expect_tx(fb, TILE_BYTES);
+          for (int hh = 0; hh < HALVES; ++hh)
+            tma_load_4d(dst + hh * kHalfBytes, tmap, fb, hh * 64, hkv, slot0, page, pol_kv);
         }
         __syncwarp();
         ++kt;
@@ -255,9 +278,9 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     } else {
       PlanSmall plan(klo_all, khi_all);
       while (!plan.done()) {
-        const int st = kt % kKvStages;
-        if (kt >= kKvStages && lane == 0)
-          ok = mbar_wait(smem_u32(&kv_empty[st]), ((kt / kKvStages) - 1) & 1, abort_flag);
+        const int st = kt % nst;
+        if (kt >= nst && lane == 0)
+          ok = mbar_wait(smem_u32(&empty[st]), ((kt / nst) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const Tile t = plan.next();
@@ -271,20 +294,17 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
           nbox += need ? 1 : 0;
         }
         if (lane == 0) {
-          const uint32_t kdst = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES);
-          const uint32_t vdst = kdst + TILE_BYTES;
-          const uint32_t fb = smem_u32(&kv_full[st]);
-          mbar_arrive_expect_tx(fb, nbox * 2 * HALVES * 16 * 128);
+          const uint32_t dst = smem_u32(ring + st * TILE_BYTES);
+          const uint32_t fb = smem_u32(&full[st]);
+          mbar_arrive_expect_tx(fb, nbox * HALVES * 16 * 128);
           for (int c = 0; c < 4; ++c) {
             const int k0 = t.jbase + 16 * c;
             if (!((k0 <= t.khi) && (k0 + 15 >= t.klo))) continue;
-            if (pages[c] < 0 || pages[c] >= p.num_pages) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
-            for (int hh = 0; hh < HALVES; ++hh) {
-              tma_load_4d(kdst + hh * kHalfBytes + c * 16 * 128, &p.tmap_k, fb, hh * 64, hkv,
-                          k0 % p.P, pages[c], pol_kv);
-              tma_load_4d(vdst + hh * kHalfBytes + c * 16 * 128, &p.tmap_v, fb, hh * 64, hkv,
-                          k0 % p.P, pages[c], pol_kv);
-            }
+            if (is_k && (pages[c] < 0 || pages[c] >= p.num_pages))
+              report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+            for (int hh = 0; hh < HALVES; ++hh)
+              tma_load_4d(dst + hh * kHalfBytes + c * 16 * 128, tmap, fb, hh * 64, hkv, k0 % p.P,
+                          pages[c], pol_kv);
           }
         }
         __syncwarp();
@@ -293,9 +313,9 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     }
     if (!ok && lane == 0) {
       report(p.dev_err, INKLING_DEVERR_TIMEOUT);
-      for (int j = max(0, kt - kKvStages); j < kt; ++j)
-        mbar_wait_drain(smem_u32(&kv_full[j % kKvStages]), (j / kKvStages) & 1);
-      mbar_wait_drain(smem_u32(q_full), 0);
+      for (int j = max(0, kt - nst); j < kt; ++j)
+        mbar_wait_drain(smem_u32(&full[j % nst]), (j / nst) & 1);
+      if (is_k) mbar_wait_drain(smem_u32(q_full), 0);
     }
   }
   // =================================================================== MMA issuer
@@ -310,8 +330,10 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       auto issue_pv = [&](int kp) -> bool {
         if (!mbar_wait(smem_u32(&p_full[kp & 1]), (kp >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
-        const int st = kp % kKvStages;
-        const uint32_t vb = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES) + TILE_BYTES;
+        const int st = kp % kVStages;
+        if (!mbar_wait(smem_u32(&v_full[st]), (kp / kVStages) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + SM::V_OFF + st * TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk) {
           const uint64_t bdesc = smem_desc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
@@ -319,7 +341,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
                     (kp > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(pv_done));
-        tc_commit(smem_u32(&kv_empty[st]));
+        tc_commit(smem_u32(&v_empty[st]));
         ++issued_pv;
         return true;
       };
@@ -342,15 +364,15 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
           }
         }
         for (k = 0; k < ntiles && ok; ++k) {
-          const int st = k % kKvStages;
-          ok = mbar_wait(smem_u32(&kv_full[st]), (k / kKvStages) & 1, abort_flag);
+          const int st = k % kKStages;
+          ok = mbar_wait(smem_u32(&k_full[st]), (k / kKStages) & 1, abort_flag);
           if (!ok) break;
           if (k >= 2) {  // S buffer k&1 is free once PV_{k-2} has read P_{k-2}
             ok = mbar_wait(smem_u32(pv_done), (k - 2) & 1, abort_flag);
             if (!ok) break;
           }
           tc_fence_after();
-          const uint32_t kb = smem_u32(smem + SM::KV_OFF + st * SM::STAGE_BYTES);
+          const uint32_t kb = smem_u32(smem + SM::K_OFF + st * TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t adesc =
@@ -360,6 +382,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
             tc_mma_ss(tmem + 64 * (k & 1), adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&s_full[k & 1]));
+          tc_commit(smem_u32(&k_empty[st]));
           if (k >= 1) ok = issue_pv(k - 1);
         }
         if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
@@ -373,80 +396,36 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     __syncwarp();
   }
   // =================================================================== softmax
-  else {
+  else if (warp >= 2 && warp < 6) {
     const int lg = warp & 3;         // TMEM lane group of this warp
     const int i = lg + 4 * lane;     // query row of this thread within the tile
     const bool valid = i < nrows;
     const int pi = pos0 + i;         // its absolute position
     const int lo_i = p.window > 0 ? max(0, pi - p.window + 1) : 0;
     const size_t row_off = ((size_t)(valid ? t0 + i : t0) * p.H_q + h) * R;
-    const float clampv = valid ? __ldg(p.rel + row_off + R - 1) * kLog2e : 0.f;
+    const float clampv = valid ? __ldg(p.rel + row_off + R - 1) : 0.f;
     const uint32_t tlane = tmem + ((uint32_t)(32 * lg) << 16);
-    const float sl2 = p.scale_log2;
-    const uint64_t pol_b = policy_evict_first();
-    float* band_base = reinterpret_cast<float*>(smem + SM::BIAS_OFF) + lg * 32 * kBiasPitch;
-    const float* my_band0 = band_base + lane * kBiasPitch;
+    const float scale = p.scale;
+    const float* my_band0 = reinterpret_cast<const float*>(smem + SM::BIAS_OFF) +
+                            lg * 32 * kBiasPitch + lane * kBiasPitch;
 
-    // copy this warp's 32 row bands of one tile into bias buffer `buf`
-    auto issue_bias = [&](const Tile& t, int buf) {
-      const uint32_t dst0 = smem_u32(band_base) + buf * kBiasBufBytes;
-#pragma unroll 4
-      for (int it = 0; it < 17; ++it) {
-        int yy, c;
-        if (it < 16) {
-          yy = 2 * it + (lane >> 4);
-          c = lane & 15;
-        } else {
-          yy = lane;
-          c = 16;
-        }
-        const int ii = lg + 4 * yy;
-        if (ii >= nrows) continue;
-        const int pp = pos0 + ii;
-        const int lo_r = p.window > 0 ? max(0, pp - p.window + 1) : 0;
-        const int vlo = max(lo_r, t.klo), vhi = min(pp, t.khi);
-        if (vlo > vhi) continue;
-        const int dtop = pp - t.jbase;
-        const int d0 = ((dtop - 63) & ~3) + 4 * c;
-        const int dmin = pp - vhi, dmax = min(pp - vlo, R - 1);
-        if (d0 + 3 < dmin || d0 > dmax) continue;
-        const float* src = p.rel + ((size_t)(t0 + ii) * p.H_q + h) * R + d0;
-        asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
-                         dst0 + (uint32_t)(yy * kBiasPitch * 4 + c * 16)),
-                     "l"(src), "l"(pol_b)
-                     : "memory");
-      }
-    };
-
-    // walk tiles: `cur` for the compute, `pre` two tiles ahead for the bias prefetch
     using PlanT = typename std::conditional<BH == 64, PlanBig, PlanSmall>::type;
-    auto make_plan = [&]() {
+    PlanT cur = [&]() {
       if constexpr (BH == 64) return PlanBig(klo_all, khi_all, p.P);
       else return PlanSmall(klo_all, khi_all);
-    };
-    auto next_tile = [&](PlanT& pl) -> Tile {
-      if constexpr (BH == 64) {
-        int lp, s0;
-        return pl.next(lp, s0);
-      } else {
-        return pl.next();
-      }
-    };
-    PlanT cur = make_plan();
-    PlanT pre = make_plan();
-    for (int j = 0; j < 2; ++j) {  // bias of tiles 0 and 1
-      if (!pre.done()) issue_bias(next_tile(pre), j);
-      cp_async_commit();
-    }
+    }();
 
-    float m_use = -INFINITY, l_sum = 0.f;
+    float m_use = -INFINITY, l_sum = 0.f;  // running max (natural units) and sum
     bool ok = true;
     int k = 0;
     for (; !cur.done(); ++k) {
-      const Tile t = next_tile(cur);
-      if (!pre.done()) issue_bias(next_tile(pre), (k + 2) % kBiasBufs);
-      cp_async_commit();
-
+      Tile t;
+      if constexpr (BH == 64) {
+        int lp, s0;
+        t = cur.next(lp, s0);
+      } else {
+        t = cur.next();
+      }
       if (!mbar_wait_warp(smem_u32(&s_full[k & 1]), (k >> 1) & 1, abort_flag)) {
         ok = false;
         break;
@@ -456,8 +435,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       tmem_ld32(tlane + 64 * (k & 1), sraw[0]);
       tmem_ld32(tlane + 64 * (k & 1) + 32, sraw[1]);
       tmem_ld_wait();
-      cp_async_wait<2>();
-      __syncwarp();
+      const int buf = k % kBiasBufs;
+      if (!mbar_wait_warp(smem_u32(&b_full[buf]), (k / kBiasBufs) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
 
       int cl = max(lo_i, t.klo) - t.jbase;
       int ch = min(pi, t.khi) - t.jbase;
@@ -469,26 +451,36 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       const bool full_vis = __all_sync(0xffffffffu, cl <= 0 && ch >= 63);
       const bool clamp = __any_sync(0xffffffffu, valid && cl <= ch && dtop - cl >= R - 1);
       const int off = (pos0 + lg - t.jbase - 63) & 3;
-      const float* band = my_band0 + (k % kBiasBufs) * (kBiasBufBytes / 4);
+      const float* band = my_band0 + buf * (kBiasBufBytes / 4);
       float s[64];
       switch (off) {
-        case 0: score_tile<0>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
-        case 1: score_tile<1>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
-        case 2: score_tile<2>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
-        default: score_tile<3>(s, sraw, band, sl2, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        case 0: score_tile<0>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        case 1: score_tile<1>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        case 2: score_tile<2>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        default: score_tile<3>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&b_empty[buf]));  // band read: the loader may refill it
 
-      float mx = -INFINITY;
+      float mx;
+      {
+        float r32[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+        for (int j = 0; j < 32; ++j) r32[j] = fmaxf(s[j], s[j + 32]);
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) r32[j] = fmaxf(r32[j], r32[j + w]);
+        mx = r32[0];
+      }
       float m_new = m_use, alpha = 1.f;
       bool resc = false;
       if (mx > -INFINITY) {
         if (m_use == -INFINITY) {
           m_new = mx;  // first visible keys of this row: its O row is still zero
-        } else if (mx > m_use + kRescaleThreshold) {
+        } else if (mx > m_use + kRescaleThreshold * kLn2) {
           m_new = mx;
-          alpha = ex2(m_use - mx);
+          alpha = ex2((m_use - mx) * kLog2e);
           resc = true;
         }
       }
@@ -512,17 +504,21 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       }
       m_use = m_new;
       l_sum *= alpha;
-      const float mu = (m_use == -INFINITY) ? 0.f : m_use;
+      const float nmu = (m_use == -INFINITY) ? 0.f : -m_use * kLog2e;
       uint32_t pk[32];
-      float sum = 0.f;
+      float ps[32];
 #pragma unroll
       for (int m = 0; m < 32; ++m) {
-        const float p0 = ex2(s[2 * m] - mu);
-        const float p1 = ex2(s[2 * m + 1] - mu);
-        sum += p0 + p1;
+        const float p0 = ex2(fmaf(s[2 * m], kLog2e, nmu));
+        const float p1 = ex2(fmaf(s[2 * m + 1], kLog2e, nmu));
+        ps[m] = p0 + p1;
         pk[m] = pack_bf16(p0, p1);
       }
-      l_sum += sum;
+#pragma unroll
+      for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
+      l_sum += ps[0];
       tmem_st32(tlane + 64 * (k & 1), pk);
       tmem_st_wait();
 
@@ -530,8 +526,12 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         // rows outside [klo, khi] may hold other keys' values (NaN included):
         // zero them in V so that P = 0 times V stays 0 in the tensor core
         const int vlo = t.klo - t.jbase, vhi = t.khi - t.jbase;
-        const int st = k % kKvStages;
-        uint8_t* vtile = smem + SM::KV_OFF + st * SM::STAGE_BYTES + TILE_BYTES;
+        const int st = k % kVStages;
+        if (!mbar_wait_warp(smem_u32(&v_full[st]), (k / kVStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* vtile = smem + SM::V_OFF + st * TILE_BYTES;
         const int sid = (warp - 2) * 32 + lane;  // 0..127
         for (int u = sid; u < 64 * HALVES * 8; u += 128) {
           const int row = u / (HALVES * 8);
@@ -546,7 +546,6 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[k & 1]));
     }
-    cp_async_wait<0>();
 
     // ---- epilogue: O / l -> bf16
     if (ok && k > 0) ok = mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag);
@@ -572,11 +571,70 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       }
       if (valid && p.lse_out)
         p.lse_out[(size_t)(t0 + i) * p.H_q + h] =
-            l_sum > 0.f ? (m_use + log2f(l_sum)) * kLn2 : -INFINITY;
+            l_sum > 0.f ? m_use + log2f(l_sum) * kLn2 : -INFINITY;
     } else if (lane == 0) {
       report(p.dev_err, INKLING_DEVERR_TIMEOUT);
     }
     tc_fence_before();
+  }
+  // =================================================================== bias loaders
+  else if (warp == 7) {
+    // warp 7: row bands of rel_logits for each key tile, one 1-D bulk copy
+    // per (row, tile): the distances the row can see in the tile, clipped to
+    // [0, R), in 16-byte chunks relative to floor4(dtop - 63)
+    const int u = lane;  // rows u, u + 32, u + 64, u + 96
+    using PlanT = typename std::conditional<BH == 64, PlanBig, PlanSmall>::type;
+    PlanT pl = [&]() {
+      if constexpr (BH == 64) return PlanBig(klo_all, khi_all, p.P);
+      else return PlanSmall(klo_all, khi_all);
+    }();
+    const uint32_t band_smem = smem_u32(smem + SM::BIAS_OFF);
+    int k = 0;
+    bool ok = true;
+    while (!pl.done()) {
+      Tile t;
+      if constexpr (BH == 64) {
+        int lp, s0;
+        t = pl.next(lp, s0);
+      } else {
+        t = pl.next();
+      }
+      const int buf = k % kBiasBufs;
+      if (k >= kBiasBufs &&
+          !mbar_wait_warp(smem_u32(&b_empty[buf]), ((k / kBiasBufs) - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = smem_u32(&b_full[buf]);
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int ii = u + 32 * rr;
+        if (ii >= nrows) continue;
+        const int pp = pos0 + ii;
+        const int lo_r = p.window > 0 ? max(0, pp - p.window + 1) : 0;
+        const int vlo = max(lo_r, t.klo), vhi = min(pp, t.khi);
+        if (vlo > vhi) continue;
+        const int dtop = pp - t.jbase;
+        const int lo4 = (dtop - 63) & ~3;
+        const int dmin = pp - vhi, dmax = min(pp - vlo, R - 1);
+        if (dmin > dmax) continue;
+        const int c_lo = (dmin - lo4) >> 2, c_hi = (dmax - lo4) >> 2;
+        const uint32_t bytes = (uint32_t)(c_hi - c_lo + 1) * 16;
+        const uint32_t dst = band_smem + buf * kBiasBufBytes + (ii & 3) * kBiasWarpBytes +
+                             (ii >> 2) * kBiasPitch * 4 + c_lo * 16;
+        const float* src = p.rel + ((size_t)(t0 + ii) * p.H_q + h) * R + lo4 + 4 * c_lo;
+        mbar_expect_tx(fb, bytes);
+        bulk_load(dst, src, bytes, fb);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fb);
+      ++k;
+    }
+    if (!ok && lane == 0) {
+      report(p.dev_err, INKLING_DEVERR_TIMEOUT);
+      for (int j = max(0, k - kBiasBufs); j < k; ++j)
+        mbar_wait_drain(smem_u32(&b_full[j % kBiasBufs]), (j / kBiasBufs) & 1);
+    }
   }
 
   __syncthreads();
@@ -651,6 +709,7 @@ int launch_prefill(const PrefillCall& c) {
   prm.max_q_len = c.max_q_len;
   prm.tiles_per_seq = std::max(1, (c.max_q_len + kQRows - 1) / kQRows);
   prm.scale_log2 = c.scale * kLog2e;
+  prm.scale = c.scale;
   if (c.max_q_len <= 0) return INKLING_OK;
   dim3 grid(c.H_q, c.B * prm.tiles_per_seq);
   if (c.D == 128)
