@@ -444,20 +444,23 @@ def barrier(args):
         torch.distributed.barrier()
 
 
-def max_over_ranks(args, x):
+def _reduce(args, x, op):
     if args.world <= 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device=f"cuda:{args.local}")
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    dev = "cpu" if torch.distributed.get_backend() == "gloo" else f"cuda:{args.local}"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=op)
     return float(t.item())
+
+
+def max_over_ranks(args, x):
+    """Slowest rank's time: the job's time."""
+    return _reduce(args, x, torch.distributed.ReduceOp.MAX) if args.world > 1 else x
 
 
 def sum_over_ranks(args, x):
-    if args.world <= 1:
-        return x
-    t = torch.tensor([x], dtype=torch.float64, device=f"cuda:{args.local}")
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
-    return float(t.item())
+    """Units processed by all ranks together."""
+    return _reduce(args, x, torch.distributed.ReduceOp.SUM) if args.world > 1 else x
 
 
 # ---------------------------------------------------------------------------

@@ -198,6 +198,17 @@ size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t H_q,
 size_t inkling_rel_attn_prefill_workspace_size(int32_t T, int32_t H_q,
                                                int32_t D);
 
+/*
+ * inkling_rel_attn_selftest_timeout -- failure-path self-test.  Launches one
+ * tiny kernel whose bounded pipeline wait (the routine every kernel of the
+ * library uses for its mbarrier waits) can never succeed: it gives up after
+ * timeout_ms milliseconds (1..10000), ORs INKLING_DEVERR_TIMEOUT into
+ * *device_error and returns, without trapping; the CUDA context stays usable.
+ * No counterpart on the pages (they describe fail-fast capability checks, vLLM
+ * #51560 "Changes", not device waits).
+ */
+int inkling_rel_attn_selftest_timeout(int32_t* device_error, int32_t timeout_ms, void* stream);
+
 /* Static, human-readable text for an INKLING_* return code. */
 const char* inkling_rel_attn_error_string(int32_t code);
 

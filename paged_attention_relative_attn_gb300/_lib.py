@@ -22,6 +22,7 @@ EXPORTED = (
     "inkling_rel_attn_choose_splits",
     "inkling_rel_attn_decode_workspace_size",
     "inkling_rel_attn_prefill_workspace_size",
+    "inkling_rel_attn_selftest_timeout",
     "inkling_rel_attn_error_string",
     "inkling_rel_attn_version",
 )
@@ -52,6 +53,7 @@ _SIGS = {
     "inkling_rel_attn_choose_splits": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "inkling_rel_attn_decode_workspace_size": (_sz, [_i32] * 8),
     "inkling_rel_attn_prefill_workspace_size": (_sz, [_i32] * 3),
+    "inkling_rel_attn_selftest_timeout": (ctypes.c_int, [_p, _i32, _p]),
     "inkling_rel_attn_error_string": (ctypes.c_char_p, [_i32]),
     "inkling_rel_attn_version": (_i32, []),
 }
@@ -124,6 +126,10 @@ def inkling_rel_attn_decode_workspace_size(B, H_q, H_kv, D, window, max_seq_len,
 
 def inkling_rel_attn_prefill_workspace_size(T, H_q, D):
     return load().inkling_rel_attn_prefill_workspace_size(T, H_q, D)
+
+
+def inkling_rel_attn_selftest_timeout(device_error, timeout_ms, stream):
+    return load().inkling_rel_attn_selftest_timeout(_v(device_error), timeout_ms, _v(stream))
 
 
 def inkling_rel_attn_error_string(code):

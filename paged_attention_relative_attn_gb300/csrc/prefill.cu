@@ -58,6 +58,8 @@ struct PrefillParams {
   CUtensorMap tmap_q[4];  // tokens r + 4y of q: {D, H_q, y}, box {64, 1, 32}
   CUtensorMap tmap_k;     // [num_pages][P][H_kv][D] bf16, box {64, 1, BH, 1}
   CUtensorMap tmap_v;
+  CUtensorMap tmap_bias;  // sheared view of rel_logits: {x col, token, row-in-group}, box {68, 1, 32}
+  int bias_tokens;        // tokens whose whole 32-row group box stays inside the tensor
   const float* rel;
   const int32_t* cu_seqlens_q;
   const int32_t* seq_lens;
@@ -85,38 +87,24 @@ struct PrefillSmem {
   static constexpr int TOTAL = BAR_OFF + NBARS * 8 + 16;
 };
 
-// Scale + bias + mask of one 64-key tile for one query row, in natural-log
-// units (s = scale * <q, k> + bias).  OFF is the
-// warp-uniform alignment of the row's band in shared memory: the bias of key
-// column c sits at float OFF + 63 - c of the band.
+// Bias of one 64-key tile for one query row, from its band in shared memory:
+// the bias of key column c sits at float OFF + 63 - c of the band, OFF being
+// the warp-uniform alignment of the band.  Only this gather differs between
+// the four alignments; all arithmetic after it is shared.
 template <int OFF>
-__device__ __forceinline__ void score_tile(float (&s)[64], const uint32_t (&sraw)[2][32],
-                                           const float* band, float scale, int cl, int ch,
-                                           bool full_vis, bool clamp, int dtop, int Rm1,
-                                           float clampv) {
+__device__ __forceinline__ void band_to_columns(float (&b)[64], const float* band) {
+  const float4* src = reinterpret_cast<const float4*>(band);
+  float bb[68];
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float bb[36];
-    const float4* src = reinterpret_cast<const float4*>(band) + (hh == 0 ? 8 : 0);
-#pragma unroll
-    for (int q = 0; q < 9; ++q) {
-      const float4 v = src[q];
-      bb[4 * q + 0] = v.x;
-      bb[4 * q + 1] = v.y;
-      bb[4 * q + 2] = v.z;
-      bb[4 * q + 3] = v.w;
-    }
-#pragma unroll
-    for (int cc = 0; cc < 32; ++cc) {
-      const int c = 32 * hh + cc;
-      const int idx = OFF + 63 - c - (hh == 0 ? 32 : 0);
-      float bv = bb[idx];
-      if (clamp) bv = (dtop - c >= Rm1) ? clampv : bv;
-      float v = fmaf(__uint_as_float(sraw[hh][cc]), scale, bv);
-      if (!full_vis) v = (c >= cl && c <= ch) ? v : -INFINITY;
-      s[c] = v;
-    }
+  for (int q = 0; q < 17; ++q) {
+    const float4 v = src[q];
+    bb[4 * q + 0] = v.x;
+    bb[4 * q + 1] = v.y;
+    bb[4 * q + 2] = v.z;
+    bb[4 * q + 3] = v.w;
   }
+#pragma unroll
+  for (int c = 0; c < 64; ++c) b[c] = bb[OFF + 63 - c];
 }
 
 template <int D, int BH>
@@ -454,11 +442,23 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       const float* band = my_band0 + buf * (kBiasBufBytes / 4);
       float s[64];
       switch (off) {
-        case 0: score_tile<0>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
-        case 1: score_tile<1>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
-        case 2: score_tile<2>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
-        default: score_tile<3>(s, sraw, band, scale, cl, ch, full_vis, clamp, dtop, R - 1, clampv); break;
+        case 0: band_to_columns<0>(s, band); break;
+        case 1: band_to_columns<1>(s, band); break;
+        case 2: band_to_columns<2>(s, band); break;
+        default: band_to_columns<3>(s, band); break;
       }
+      // scale + bias (+ clamp) + mask, natural-log units
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) {
+          const int c = 32 * hh + cc;
+          float bv = s[c];
+          if (clamp) bv = (dtop - c >= R - 1) ? clampv : bv;
+          float v = fmaf(__uint_as_float(sraw[hh][cc]), scale, bv);
+          if (!full_vis) v = (c >= cl && c <= ch) ? v : -INFINITY;
+          s[c] = v;
+        }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&b_empty[buf]));  // band read: the loader may refill it
 
@@ -579,10 +579,13 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   }
   // =================================================================== bias loaders
   else if (warp == 7) {
-    // warp 7: row bands of rel_logits for each key tile, one 1-D bulk copy
-    // per (row, tile): the distances the row can see in the tile, clipped to
-    // [0, R), in 16-byte chunks relative to floor4(dtop - 63)
-    const int u = lane;  // rows u, u + 32, u + 64, u + 96
+    // warp 7: the row bands of rel_logits for each key tile.  Row y of lane
+    // group j is query token t0 + j + 4y; its band is the 68 floats of its
+    // bias row starting at floor4(dtop - 63), dtop = its position - jbase.
+    // Within a group the band start moves by exactly 4 floats per row, so one
+    // TMA box of a sheared view (token stride plus 4 floats per row) loads the
+    // whole group.
+    const uint64_t pol_b = policy_evict_first();
     using PlanT = typename std::conditional<BH == 64, PlanBig, PlanSmall>::type;
     PlanT pl = [&]() {
       if constexpr (BH == 64) return PlanBig(klo_all, khi_all, p.P);
@@ -606,25 +609,43 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         break;
       }
       const uint32_t fb = smem_u32(&b_full[buf]);
+      const uint32_t buf_smem = band_smem + buf * kBiasBufBytes;
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int ii = u + 32 * rr;
-        if (ii >= nrows) continue;
-        const int pp = pos0 + ii;
-        const int lo_r = p.window > 0 ? max(0, pp - p.window + 1) : 0;
-        const int vlo = max(lo_r, t.klo), vhi = min(pp, t.khi);
-        if (vlo > vhi) continue;
-        const int dtop = pp - t.jbase;
-        const int lo4 = (dtop - 63) & ~3;
-        const int dmin = pp - vhi, dmax = min(pp - vlo, R - 1);
-        if (dmin > dmax) continue;
-        const int c_lo = (dmin - lo4) >> 2, c_hi = (dmax - lo4) >> 2;
-        const uint32_t bytes = (uint32_t)(c_hi - c_lo + 1) * 16;
-        const uint32_t dst = band_smem + buf * kBiasBufBytes + (ii & 3) * kBiasWarpBytes +
-                             (ii >> 2) * kBiasPitch * 4 + c_lo * 16;
-        const float* src = p.rel + ((size_t)(t0 + ii) * p.H_q + h) * R + lo4 + 4 * c_lo;
-        mbar_expect_tx(fb, bytes);
-        bulk_load(dst, src, bytes, fb);
+      for (int j = 0; j < 4; ++j) {  // row group j: rows j + 4y = tokens t0 + j + 4y
+        if (j >= nrows) continue;
+        const int tf = t0 + j;
+        const int lo4_0 = (pos0 + j - t.jbase - 63) & ~3;
+        // the map's bounds are checked on the sheared x: a negative x would
+        // zero-fill entries whose true column x + 4y is valid, so such boxes
+        // take the per-row path too
+        if (tf < p.bias_tokens && h * R + lo4_0 >= 0) {
+          // one box of the sheared view: row y of the group starts 4y floats
+          // later than row 0, exactly the shift of its band
+          if (lane == 0) {
+            const int lo4 = lo4_0;
+            mbar_expect_tx(fb, 32 * kBiasPitch * 4);
+            tma_load_3d(buf_smem + j * kBiasWarpBytes, &p.tmap_bias, fb, h * R + lo4, tf, 0,
+                        pol_b);
+          }
+        } else {
+          // the box could reach past the end of the tensor: per-row copies
+          const int ii = j + 4 * lane;
+          if (ii >= nrows) continue;
+          const int pp = pos0 + ii;
+          const int lo_r = p.window > 0 ? max(0, pp - p.window + 1) : 0;
+          const int vlo = max(lo_r, t.klo), vhi = min(pp, t.khi);
+          if (vlo > vhi) continue;
+          const int dtop = pp - t.jbase;
+          const int lo4 = (dtop - 63) & ~3;
+          const int dmin = pp - vhi, dmax = min(pp - vlo, R - 1);
+          if (dmin > dmax) continue;
+          const int c_lo = (dmin - lo4) >> 2, c_hi = (dmax - lo4) >> 2;
+          const uint32_t bytes = (uint32_t)(c_hi - c_lo + 1) * 16;
+          const uint32_t dst = buf_smem + j * kBiasWarpBytes + lane * kBiasPitch * 4 + c_lo * 16;
+          const float* src = p.rel + ((size_t)(t0 + ii) * p.H_q + h) * R + lo4 + 4 * c_lo;
+          mbar_expect_tx(fb, bytes);
+          bulk_load(dst, src, bytes, fb);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);
@@ -687,6 +708,23 @@ int launch_prefill(const PrefillCall& c) {
       return INKLING_ERR_CUDA;
     if (!encode_tiled(&prm.tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(c.v_cache),
                       dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return INKLING_ERR_CUDA;
+  }
+  {
+    // sheared view of rel_logits [T][H_q][R] fp32: element (x, z, y) at
+    // rel + z*H_q*R + y*(4*H_q*R + 4) + x  -- token z + 4y, column x + 4y.
+    // Tokens z past bias_tokens are out of the map (their boxes use per-row
+    // copies), so no box ever touches memory past the end of the tensor.
+    const uint64_t row = (uint64_t)c.H_q * c.R;
+    // (needs rows of at least 64 floats so that the 124-float shear of the
+    // last box row stays inside the following token row)
+    const int64_t ok_tokens = row >= 64 ? (int64_t)c.T - 126 : 0;
+    prm.bias_tokens = (int)std::max<int64_t>(0, ok_tokens);
+    uint64_t dims[3] = {row, (uint64_t)std::max<int64_t>(1, ok_tokens), 32};
+    uint64_t strides[2] = {row * 4, (4 * row + 4) * 4};
+    uint32_t box[3] = {(uint32_t)kBiasPitch, 1, 32};
+    if (!encode_tiled(&prm.tmap_bias, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                      const_cast<float*>(c.rel), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return INKLING_ERR_CUDA;
   }
   prm.rel = c.rel;
