@@ -33,11 +33,13 @@ struct Tile {
 // zero-filled.  So only visible keys' bytes are fetched; only a range that
 // starts and ends inside one page loads a few in-bounds rows past its end.
 struct PlanBig {
-  int e, P, jt;
-  __device__ PlanBig(int a, int e_, int P_) : e(e_), P(P_), jt(a) {}
+  int e, P, jt, lp2;  // lp2 = log2(P) when P is a power of two, else -1
+  __device__ PlanBig(int a, int e_, int P_) : e(e_), P(P_), jt(a) {
+    lp2 = (P_ & (P_ - 1)) == 0 ? __ffs(P_) - 1 : -1;
+  }
   __device__ bool done() const { return jt > e; }
   __device__ Tile next(int& lpage, int& slot0) {
-    const int lp = jt / P;
+    const int lp = lp2 >= 0 ? (jt >> lp2) : jt / P;
     const int pstart = lp * P;
     const int pe = pstart + P - 1;
     int et = min(jt + 63, pe);

@@ -15,8 +15,8 @@
 //    memory, K-major) and O += P_{k-1} V_{k-1} (A = P from tensor memory, B = V
 //    MN-major from shared memory), so QK^T of tile k overlaps the softmax of
 //    tile k-1;
-//  * warps 2-5 are the softmax warpgroup: thread = one query row = one TMEM
-//    lane.  They read S with tcgen05.ld, add the bias, apply the causal /
+//  * warps 2-5 and 8-11 are two softmax warpgroups: a thread owns one query
+//    row (one TMEM lane) and one half of the key columns of each tile.  They read S with tcgen05.ld, add the bias, apply the causal /
 //    window mask, keep the running max lazily (O is rescaled in tensor memory
 //    only when the max grows by more than 2^8), write P (bf16) back into the S
 //    columns with tcgen05.st, and finally normalise O and store it.
@@ -44,7 +44,7 @@
 
 namespace ira {
 
-constexpr int kPrefThreads = 256;
+constexpr int kPrefThreads = 384;
 constexpr int kQRows = 128;
 constexpr int kKStages = 3;  // K tiles: released when QK^T has read them
 constexpr int kVStages = 2;  // V tiles: released when PV has read them
@@ -81,22 +81,26 @@ struct PrefillSmem {
   static constexpr int K_OFF = Q_BYTES;
   static constexpr int V_OFF = K_OFF + kKStages * TILE_BYTES;
   static constexpr int BIAS_OFF = V_OFF + kVStages * TILE_BYTES;
-  static constexpr int BAR_OFF = BIAS_OFF + kBiasBufs * kBiasBufBytes;
-  // q_full, k_full/empty, v_full/empty, s_full[2], p_full[2], pv_done, b_full/empty
-  static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 2 * kBiasBufs;
+  static constexpr int X_OFF = BIAS_OFF + kBiasBufs * kBiasBufBytes;  // row exchange [2][2][128]
+  static constexpr int BAR_OFF = X_OFF + 2 * 2 * kQRows * 4;
+  // q_full, k_full/empty, v_full/empty, s_full[2], p_full[2], pv_done, b_full/empty, x_bar[4]
+  static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 2 * kBiasBufs + 4;
   static constexpr int TOTAL = BAR_OFF + NBARS * 8 + 16;
 };
 
-// Bias of one 64-key tile for one query row, from its band in shared memory:
-// the bias of key column c sits at float OFF + 63 - c of the band, OFF being
-// the warp-uniform alignment of the band.  Only this gather differs between
-// the four alignments; all arithmetic after it is shared.
+// Scores of one column half (32 keys) of a 64-key tile for one query row:
+// s[cc] = scale * S[cc] + bias, the bias read from the row's band in shared
+// memory.  `half_band` points at the part of the band holding this half's 32
+// distances (+3); key column cc of the half sits at float OFF + 31 - cc, OFF
+// being the warp-uniform alignment of the band.  Only this gather differs
+// between the four alignments.
 template <int OFF>
-__device__ __forceinline__ void band_to_columns(float (&b)[64], const float* band) {
-  const float4* src = reinterpret_cast<const float4*>(band);
-  float bb[68];
+__device__ __forceinline__ void half_scores(float (&s)[32], const uint32_t (&sraw)[32],
+                                            const float* half_band, float scale) {
+  const float4* src = reinterpret_cast<const float4*>(half_band);
+  float bb[36];
 #pragma unroll
-  for (int q = 0; q < 17; ++q) {
+  for (int q = 0; q < 9; ++q) {
     const float4 v = src[q];
     bb[4 * q + 0] = v.x;
     bb[4 * q + 1] = v.y;
@@ -104,7 +108,7 @@ __device__ __forceinline__ void band_to_columns(float (&b)[64], const float* ban
     bb[4 * q + 3] = v.w;
   }
 #pragma unroll
-  for (int c = 0; c < 64; ++c) b[c] = bb[OFF + 63 - c];
+  for (int cc = 0; cc < 32; ++cc) s[cc] = fmaf(__uint_as_float(sraw[cc]), scale, bb[OFF + 31 - cc]);
 }
 
 template <int D, int BH>
@@ -163,7 +167,8 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   uint64_t* pv_done = p_full + 2;
   uint64_t* b_full = pv_done + 1;
   uint64_t* b_empty = b_full + kBiasBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_empty + kBiasBufs);
+  uint64_t* x_bar = b_empty + kBiasBufs;  // per lane group: the two softmax warps of a row
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_bar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (tid == 0) {
@@ -178,12 +183,13 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&p_full[s]), 4);
+      mbar_init(smem_u32(&p_full[s]), 8);  // the eight softmax warps
     }
+    for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&x_bar[s]), 2);
     mbar_init(smem_u32(pv_done), 1);
     for (int s = 0; s < kBiasBufs; ++s) {
       mbar_init(smem_u32(&b_full[s]), 1);   // the bias loader warp
-      mbar_init(smem_u32(&b_empty[s]), 4);  // the four softmax warps
+      mbar_init(smem_u32(&b_empty[s]), 8);  // the eight softmax warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -384,7 +390,13 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     __syncwarp();
   }
   // =================================================================== softmax
-  else if (warp >= 2 && warp < 6) {
+  else if ((warp >= 2 && warp < 6) || warp >= 8) {
+    // Two warpgroups share every row: warps 2-5 take key columns 0..31 of
+    // each tile, warps 8-11 columns 32..63 (and the matching halves of P, of
+    // the O rescale and of the output).  The two warps of a row exchange
+    // their partial row max (and at the end their partial sums) through
+    // shared memory, paired by an mbarrier.
+    const int grp = warp >= 8 ? 1 : 0;
     const int lg = warp & 3;         // TMEM lane group of this warp
     const int i = lg + 4 * lane;     // query row of this thread within the tile
     const bool valid = i < nrows;
@@ -394,8 +406,10 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     const float clampv = valid ? __ldg(p.rel + row_off + R - 1) : 0.f;
     const uint32_t tlane = tmem + ((uint32_t)(32 * lg) << 16);
     const float scale = p.scale;
-    const float* my_band0 = reinterpret_cast<const float*>(smem + SM::BIAS_OFF) +
-                            lg * 32 * kBiasPitch + lane * kBiasPitch;
+    const float* my_half0 = reinterpret_cast<const float*>(smem + SM::BIAS_OFF) +
+                            lg * 32 * kBiasPitch + lane * kBiasPitch + 32 * (1 - grp);
+    float* xbuf = reinterpret_cast<float*>(smem + SM::X_OFF);  // [2 parity][2 grp][128 rows]
+    const int c0 = 32 * grp;  // first key column of this half
 
     using PlanT = typename std::conditional<BH == 64, PlanBig, PlanSmall>::type;
     PlanT cur = [&]() {
@@ -403,7 +417,17 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       else return PlanSmall(klo_all, khi_all);
     }();
 
-    float m_use = -INFINITY, l_sum = 0.f;  // running max (natural units) and sum
+    // exchange one float per row with the partner warp (phase n of x_bar[lg])
+    auto exchange = [&](int n, float mine) -> float {
+      float* xb = xbuf + (n & 1) * 256;
+      xb[grp * 128 + i] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&x_bar[lg]));
+      if (!mbar_wait_warp(smem_u32(&x_bar[lg]), n & 1, abort_flag)) return NAN;
+      return xb[(1 - grp) * 128 + i];
+    };
+
+    float m_use = -INFINITY, l_part = 0.f;  // running max (natural units), sum of my half
     bool ok = true;
     int k = 0;
     for (; !cur.done(); ++k) {
@@ -419,60 +443,63 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sraw[2][32];
-      tmem_ld32(tlane + 64 * (k & 1), sraw[0]);
-      tmem_ld32(tlane + 64 * (k & 1) + 32, sraw[1]);
+      uint32_t sraw[32];
+      tmem_ld32(tlane + 64 * (k & 1) + c0, sraw);
       tmem_ld_wait();
       const int buf = k % kBiasBufs;
       if (!mbar_wait_warp(smem_u32(&b_full[buf]), (k / kBiasBufs) & 1, abort_flag)) {
         ok = false;
         break;
       }
-
+      // visible key columns of this row in this tile, and in my half
       int cl = max(lo_i, t.klo) - t.jbase;
       int ch = min(pi, t.khi) - t.jbase;
       if (!valid) {
         cl = 64;
         ch = -1;
       }
+      const int hl = max(cl, c0), hh = min(ch, c0 + 31);
       const int dtop = pi - t.jbase;
-      const bool full_vis = __all_sync(0xffffffffu, cl <= 0 && ch >= 63);
-      const bool clamp = __any_sync(0xffffffffu, valid && cl <= ch && dtop - cl >= R - 1);
+      const bool full_vis = __all_sync(0xffffffffu, hl == c0 && hh == c0 + 31);
+      const bool clamp = __any_sync(0xffffffffu, valid && hl <= hh && dtop - hl >= R - 1);
       const int off = (pos0 + lg - t.jbase - 63) & 3;
-      const float* band = my_band0 + buf * (kBiasBufBytes / 4);
-      float s[64];
+      const float* half_band = my_half0 + buf * (kBiasBufBytes / 4);
+      float s[32];
       switch (off) {
-        case 0: band_to_columns<0>(s, band); break;
-        case 1: band_to_columns<1>(s, band); break;
-        case 2: band_to_columns<2>(s, band); break;
-        default: band_to_columns<3>(s, band); break;
+        case 0: half_scores<0>(s, sraw, half_band, scale); break;
+        case 1: half_scores<1>(s, sraw, half_band, scale); break;
+        case 2: half_scores<2>(s, sraw, half_band, scale); break;
+        default: half_scores<3>(s, sraw, half_band, scale); break;
       }
-      // scale + bias (+ clamp) + mask, natural-log units
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
-          const int c = 32 * hh + cc;
-          float bv = s[c];
-          if (clamp) bv = (dtop - c >= R - 1) ? clampv : bv;
-          float v = fmaf(__uint_as_float(sraw[hh][cc]), scale, bv);
-          if (!full_vis) v = (c >= cl && c <= ch) ? v : -INFINITY;
-          s[c] = v;
-        }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&b_empty[buf]));  // band read: the loader may refill it
+      if (clamp) {  // distances >= R - 1 share the table's last column
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+          if (dtop - (c0 + cc) >= R - 1) s[cc] = fmaf(__uint_as_float(sraw[cc]), scale, clampv);
+      }
+      if (!full_vis) {
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) s[cc] = (c0 + cc >= cl && c0 + cc <= ch) ? s[cc] : -INFINITY;
+      }
 
       float mx;
       {
-        float r32[32];
+        float r16[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r32[j] = fmaxf(s[j], s[j + 32]);
+        for (int j = 0; j < 16; ++j) r16[j] = fmaxf(s[j], s[j + 16]);
 #pragma unroll
-        for (int w = 16; w >= 1; w >>= 1)
+        for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
-          for (int j = 0; j < w; ++j) r32[j] = fmaxf(r32[j], r32[j + w]);
-        mx = r32[0];
+          for (int j = 0; j < w; ++j) r16[j] = fmaxf(r16[j], r16[j + w]);
+        mx = r16[0];
       }
+      const float other = exchange(k, mx);
+      if (other != other) {  // NaN: the pairing wait gave up
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, other);
       float m_new = m_use, alpha = 1.f;
       bool resc = false;
       if (mx > -INFINITY) {
@@ -485,55 +512,58 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         }
       }
       if (__any_sync(0xffffffffu, resc)) {
-        // O holds PV_0..PV_{k-1}; wait for the last one, then rescale in place
+        // O holds PV_0..PV_{k-1}; wait for the last one, then rescale my half
         if (!mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tlane + kOCol + 32 * cc, o);
+          const uint32_t col = tlane + kOCol + (D / 2) * grp + 32 * cc;
+          tmem_ld32(col, o);
           tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tmem_st32(tlane + kOCol + 32 * cc, o);
+          tmem_st32(col, o);
         }
         tmem_st_wait();
       }
       m_use = m_new;
-      l_sum *= alpha;
+      l_part *= alpha;
       const float nmu = (m_use == -INFINITY) ? 0.f : -m_use * kLog2e;
-      uint32_t pk[32];
-      float ps[32];
+      uint32_t pk[16];
+      float ps[16];
 #pragma unroll
-      for (int m = 0; m < 32; ++m) {
+      for (int m = 0; m < 16; ++m) {
         const float p0 = ex2(fmaf(s[2 * m], kLog2e, nmu));
         const float p1 = ex2(fmaf(s[2 * m + 1], kLog2e, nmu));
         ps[m] = p0 + p1;
         pk[m] = pack_bf16(p0, p1);
       }
 #pragma unroll
-      for (int w = 16; w >= 1; w >>= 1)
+      for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
-      l_sum += ps[0];
-      tmem_st32(tlane + 64 * (k & 1), pk);
+      l_part += ps[0];
+      // P (bf16 pairs) over the first 32 columns of the S buffer; both halves
+      // read their S columns before the exchange above, so no write races a read
+      tmem_st16(tlane + 64 * (k & 1) + 16 * grp, pk);
       tmem_st_wait();
 
       if (t.dirty) {
         // rows outside [klo, khi] may hold other keys' values (NaN included):
         // zero them in V so that P = 0 times V stays 0 in the tensor core
-        const int vlo = t.klo - t.jbase, vhi = t.khi - t.jbase;
         const int st = k % kVStages;
         if (!mbar_wait_warp(smem_u32(&v_full[st]), (k / kVStages) & 1, abort_flag)) {
           ok = false;
           break;
         }
+        const int vlo = t.klo - t.jbase, vhi = t.khi - t.jbase;
         uint8_t* vtile = smem + SM::V_OFF + st * TILE_BYTES;
-        const int sid = (warp - 2) * 32 + lane;  // 0..127
-        for (int u = sid; u < 64 * HALVES * 8; u += 128) {
+        const int sid = grp * 128 + lg * 32 + lane;  // 0..255
+        for (int u = sid; u < 64 * HALVES * 8; u += 256) {
           const int row = u / (HALVES * 8);
           const int rest = u - row * HALVES * 8;
           if (row >= vlo && row <= vhi) continue;
@@ -547,16 +577,22 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&p_full[k & 1]));
     }
 
-    // ---- epilogue: O / l -> bf16
+    // ---- epilogue: O / l -> bf16, each warpgroup its half of the columns
+    float l_sum = l_part;
+    if (ok) {
+      const float other = exchange(k, l_part);
+      if (other != other) ok = false;
+      else l_sum += other;
+    }
     if (ok && k > 0) ok = mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag);
     if (ok) {
       tc_fence_after();
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      __nv_bfloat16* orow = p.out + ((size_t)(t0 + i) * p.H_q + h) * D;
+      __nv_bfloat16* orow = p.out + ((size_t)(t0 + i) * p.H_q + h) * D + (D / 2) * grp;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tlane + kOCol + 32 * cc, o);
+        tmem_ld32(tlane + kOCol + (D / 2) * grp + 32 * cc, o);
         tmem_ld_wait();
         if (valid) {
           uint32_t pkd[16];
@@ -569,7 +605,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
             dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
         }
       }
-      if (valid && p.lse_out)
+      if (valid && grp == 0 && p.lse_out)
         p.lse_out[(size_t)(t0 + i) * p.H_q + h] =
             l_sum > 0.f ? m_use + log2f(l_sum) * kLn2 : -INFINITY;
     } else if (lane == 0) {
