@@ -10,7 +10,8 @@
 //  * warp 0 loads the Q tile once (TMA) and walks the tile's visible key range
 //    in page-respecting tiles of 64 keys (TMA of K and V, 128-byte swizzle,
 //    2-stage ring), exactly like the decode kernel;
-//  * warp 1 owns tensor memory (S double buffer 2 x 64 columns + O, D columns)
+//  * warp 1 owns tensor memory (S double buffer 2 x 64 columns, and two O
+//    accumulators of D columns, one per half of the key columns)
 //    and one of its threads issues the MMAs: S_k = Q K_k^T (A and B from shared
 //    memory, K-major) and O += P_{k-1} V_{k-1} (A = P from tensor memory, B = V
 //    MN-major from shared memory), so QK^T of tile k overlaps the softmax of
@@ -83,8 +84,9 @@ struct PrefillSmem {
   static constexpr int BIAS_OFF = V_OFF + kVStages * TILE_BYTES;
   static constexpr int X_OFF = BIAS_OFF + kBiasBufs * kBiasBufBytes;  // row exchange [2][2][128]
   static constexpr int BAR_OFF = X_OFF + 2 * 2 * kQRows * 4;
-  // q_full, k_full/empty, v_full/empty, s_full[2], p_full[2], pv_done, b_full/empty, x_bar[4]
-  static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 2 * kBiasBufs + 4;
+  // q_full, k_full/empty, v_full/empty, s_full[2], p_full[2], pv_done, b_full/empty, x_bar[4],
+  // o_done
+  static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 2 * kBiasBufs + 4 + 1;
   static constexpr int TOTAL = BAR_OFF + NBARS * 8 + 16;
 };
 
@@ -117,8 +119,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   using SM = PrefillSmem<D>;
   constexpr int HALVES = SM::HALVES;
   constexpr int TILE_BYTES = SM::TILE_BYTES;
-  constexpr uint32_t kTmemCols = 256;  // S0 [0,64) S1 [64,128) O [128, 128+D)
+  // S0 [0,64) S1 [64,128); O_A [128, 128+D) accumulates key columns 0..31 of
+  // every tile, O_B [256, 256+D) columns 32..63 (merged in the epilogue)
+  constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kOCol = 128;
+  constexpr uint32_t kOHalfStride = 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -168,7 +173,12 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   uint64_t* b_full = pv_done + 1;
   uint64_t* b_empty = b_full + kBiasBufs;
   uint64_t* x_bar = b_empty + kBiasBufs;  // per lane group: the two softmax warps of a row
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_bar + 4);
+  // every MMA of the CTA has completed (one phase, committed after the last PV).
+  // The softmax warps cannot use pv_done for this: one half may reach its
+  // epilogue while PV_{n-2} is still pending, and phase n-1 has the parity of
+  // phase n-3.
+  uint64_t* o_done = x_bar + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (tid == 0) {
@@ -187,6 +197,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     }
     for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&x_bar[s]), 2);
     mbar_init(smem_u32(pv_done), 1);
+    mbar_init(smem_u32(o_done), 1);
     for (int s = 0; s < kBiasBufs; ++s) {
       mbar_init(smem_u32(&b_full[s]), 1);   // the bias loader warp
       mbar_init(smem_u32(&b_empty[s]), 8);  // the eight softmax warps
@@ -320,7 +331,6 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       const uint32_t q_base = smem_u32(smem);
       bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag);
       tc_fence_after();
-      int issued_pv = 0;  // PV MMAs issued (== completed phases of pv_done once waited)
       auto issue_pv = [&](int kp) -> bool {
         if (!mbar_wait(smem_u32(&p_full[kp & 1]), (kp >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
@@ -329,14 +339,16 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + SM::V_OFF + st * TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {
+        for (int kk = 0; kk < kTileRows / 16; ++kk) {  // keys 16kk..16kk+15
           const uint64_t bdesc = smem_desc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
-          tc_mma_ts(tmem + kOCol, tmem + 64 * (kp & 1) + 8 * kk, bdesc, idesc_pv,
-                    (kp > 0 || kk > 0) ? 1u : 0u);
+          // keys 0..31 -> O_A with P at S columns 0..15; keys 32..63 -> O_B with
+          // P at S columns 32..47
+          const uint32_t o = tmem + kOCol + (kk >= 2 ? kOHalfStride : 0);
+          const uint32_t a = tmem + 64 * (kp & 1) + (kk >= 2 ? 32 + 8 * (kk - 2) : 8 * kk);
+          tc_mma_ts(o, a, bdesc, idesc_pv, (kp > 0 || (kk & 1)) ? 1u : 0u);
         }
         tc_commit(smem_u32(pv_done));
         tc_commit(smem_u32(&v_empty[st]));
-        ++issued_pv;
         return true;
       };
       int k = 0;
@@ -381,10 +393,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         }
         if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
       }
+      tc_commit(smem_u32(o_done));  // arrives once every MMA issued above has completed
       if (!ok) {
         report(p.dev_err, INKLING_DEVERR_TIMEOUT);
         // let the MMAs already issued finish before tensor memory is released
-        if (issued_pv > 0) mbar_wait_drain(smem_u32(pv_done), (issued_pv - 1) & 1);
+        mbar_wait_drain(smem_u32(o_done), 0);
       }
     }
     __syncwarp();
@@ -392,10 +405,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   // =================================================================== softmax
   else if ((warp >= 2 && warp < 6) || warp >= 8) {
     // Two warpgroups share every row: warps 2-5 take key columns 0..31 of
-    // each tile, warps 8-11 columns 32..63 (and the matching halves of P, of
-    // the O rescale and of the output).  The two warps of a row exchange
-    // their partial row max (and at the end their partial sums) through
-    // shared memory, paired by an mbarrier.
+    // each tile, warps 8-11 columns 32..63.  Each half runs its own online
+    // softmax (max, sum) into its own O accumulator in tensor memory, so the
+    // two never wait on each other inside the key loop; the epilogue merges
+    // the halves (exchange of (m, l) through shared memory, paired by an
+    // mbarrier) and each warpgroup writes half of the output columns.
     const int grp = warp >= 8 ? 1 : 0;
     const int lg = warp & 3;         // TMEM lane group of this warp
     const int i = lg + 4 * lane;     // query row of this thread within the tile
@@ -405,10 +419,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     const size_t row_off = ((size_t)(valid ? t0 + i : t0) * p.H_q + h) * R;
     const float clampv = valid ? __ldg(p.rel + row_off + R - 1) : 0.f;
     const uint32_t tlane = tmem + ((uint32_t)(32 * lg) << 16);
+    const uint32_t o_mine = tlane + kOCol + kOHalfStride * grp;
     const float scale = p.scale;
     const float* my_half0 = reinterpret_cast<const float*>(smem + SM::BIAS_OFF) +
                             lg * 32 * kBiasPitch + lane * kBiasPitch + 32 * (1 - grp);
-    float* xbuf = reinterpret_cast<float*>(smem + SM::X_OFF);  // [2 parity][2 grp][128 rows]
+    float* xbuf = reinterpret_cast<float*>(smem + SM::X_OFF);  // [2 value][2 grp][128 rows]
     const int c0 = 32 * grp;  // first key column of this half
 
     using PlanT = typename std::conditional<BH == 64, PlanBig, PlanSmall>::type;
@@ -417,17 +432,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       else return PlanSmall(klo_all, khi_all);
     }();
 
-    // exchange one float per row with the partner warp (phase n of x_bar[lg])
-    auto exchange = [&](int n, float mine) -> float {
-      float* xb = xbuf + (n & 1) * 256;
-      xb[grp * 128 + i] = mine;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&x_bar[lg]));
-      if (!mbar_wait_warp(smem_u32(&x_bar[lg]), n & 1, abort_flag)) return NAN;
-      return xb[(1 - grp) * 128 + i];
-    };
-
-    float m_use = -INFINITY, l_part = 0.f;  // running max (natural units), sum of my half
+    float m_use = -INFINITY, l_part = 0.f;  // this half's running max (natural units) and sum
     bool ok = true;
     int k = 0;
     for (; !cur.done(); ++k) {
@@ -494,17 +499,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
           for (int j = 0; j < w; ++j) r16[j] = fmaxf(r16[j], r16[j + w]);
         mx = r16[0];
       }
-      const float other = exchange(k, mx);
-      if (other != other) {  // NaN: the pairing wait gave up
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, other);
       float m_new = m_use, alpha = 1.f;
       bool resc = false;
       if (mx > -INFINITY) {
         if (m_use == -INFINITY) {
-          m_new = mx;  // first visible keys of this row: its O row is still zero
+          m_new = mx;  // first visible keys of this row in my half: my O row is still zero
         } else if (mx > m_use + kRescaleThreshold * kLn2) {
           m_new = mx;
           alpha = ex2((m_use - mx) * kLog2e);
@@ -512,21 +511,20 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         }
       }
       if (__any_sync(0xffffffffu, resc)) {
-        // O holds PV_0..PV_{k-1}; wait for the last one, then rescale my half
+        // my O holds PV_0..PV_{k-1}; wait for the last one, then rescale it
         if (!mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
-          const uint32_t col = tlane + kOCol + (D / 2) * grp + 32 * cc;
-          tmem_ld32(col, o);
+          tmem_ld32(o_mine + 32 * cc, o);
           tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tmem_st32(col, o);
+          tmem_st32(o_mine + 32 * cc, o);
         }
         tmem_st_wait();
       }
@@ -547,9 +545,9 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
       l_part += ps[0];
-      // P (bf16 pairs) over the first 32 columns of the S buffer; both halves
-      // read their S columns before the exchange above, so no write races a read
-      tmem_st16(tlane + 64 * (k & 1) + 16 * grp, pk);
+      // my half of P (16 bf16 pairs) over the first 16 of my own S columns
+      // (which I have already read): half A at columns 0..15, half B at 32..47
+      tmem_st16(tlane + 64 * (k & 1) + c0, pk);
       tmem_st_wait();
 
       if (t.dirty) {
@@ -577,28 +575,43 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&p_full[k & 1]));
     }
 
-    // ---- epilogue: O / l -> bf16, each warpgroup its half of the columns
-    float l_sum = l_part;
+    // ---- epilogue: merge the two halves, O / l -> bf16 (half the columns each)
+    if (ok && k > 0) ok = mbar_wait_warp(smem_u32(o_done), 0, abort_flag);
+    float M = m_use, L = l_part, sc_a = 1.f, sc_b = 0.f;
     if (ok) {
-      const float other = exchange(k, l_part);
-      if (other != other) ok = false;
-      else l_sum += other;
+      xbuf[(0 * 2 + grp) * 128 + i] = m_use;
+      xbuf[(1 * 2 + grp) * 128 + i] = l_part;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&x_bar[lg]));
+      ok = mbar_wait_warp(smem_u32(&x_bar[lg]), 0, abort_flag);
+      if (ok) {
+        const float ma = xbuf[(0 * 2 + 0) * 128 + i], mb = xbuf[(0 * 2 + 1) * 128 + i];
+        const float la = xbuf[(1 * 2 + 0) * 128 + i], lb = xbuf[(1 * 2 + 1) * 128 + i];
+        M = fmaxf(ma, mb);
+        sc_a = M == -INFINITY ? 0.f : ex2((ma - M) * kLog2e);
+        sc_b = M == -INFINITY ? 0.f : ex2((mb - M) * kLog2e);
+        L = sc_a * la + sc_b * lb;
+      }
     }
-    if (ok && k > 0) ok = mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag);
     if (ok) {
       tc_fence_after();
-      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      sc_a *= inv;
+      sc_b *= inv;
       __nv_bfloat16* orow = p.out + ((size_t)(t0 + i) * p.H_q + h) * D + (D / 2) * grp;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tlane + kOCol + (D / 2) * grp + 32 * cc, o);
+        uint32_t oa[32], ob[32];
+        tmem_ld32(tlane + kOCol + (D / 2) * grp + 32 * cc, oa);
+        tmem_ld32(tlane + kOCol + kOHalfStride + (D / 2) * grp + 32 * cc, ob);
         tmem_ld_wait();
         if (valid) {
           uint32_t pkd[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x)
-            pkd[x] = pack_bf16(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+            pkd[x] = pack_bf16(
+                fmaf(__uint_as_float(oa[2 * x]), sc_a, __uint_as_float(ob[2 * x]) * sc_b),
+                fmaf(__uint_as_float(oa[2 * x + 1]), sc_a, __uint_as_float(ob[2 * x + 1]) * sc_b));
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
 #pragma unroll
           for (int x = 0; x < 4; ++x)
@@ -606,8 +619,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         }
       }
       if (valid && grp == 0 && p.lse_out)
-        p.lse_out[(size_t)(t0 + i) * p.H_q + h] =
-            l_sum > 0.f ? m_use + log2f(l_sum) * kLn2 : -INFINITY;
+        p.lse_out[(size_t)(t0 + i) * p.H_q + h] = L > 0.f ? M + log2f(L) * kLn2 : -INFINITY;
     } else if (lane == 0) {
       report(p.dev_err, INKLING_DEVERR_TIMEOUT);
     }
