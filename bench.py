@@ -275,7 +275,8 @@ def bench_prefill(args, device, K, warmup):
     chunks = []
     cache = None
     for c in range(4):
-        inp, cache = W.make_chunked_prefill(c, device=device, seed=0, cache=cache)
+        inp, cache = W.make_chunked_prefill(c, device=device, seed=0, cache=cache,
+                                            n_seqs=args.batch)
         chunks.append(inp)
     work = [prefill_work(x, x.window) for x in chunks]
     outs = [torch.empty_like(x.q) for x in chunks]
@@ -289,10 +290,10 @@ def bench_prefill(args, device, K, warmup):
     flops = K * sum(w[0] for w in work)
     nbytes = K * sum(w[1] for w in work)
     x0 = chunks[0]
-    config = {"workload": "chunked_prefill", "sequences": 4, "seq_len": 8192, "chunk": 2048,
+    config = {"workload": "chunked_prefill", "sequences": x0.B, "seq_len": 8192, "chunk": 2048,
               "tokens_per_call": x0.T, "heads": f"{x0.H_q}/{x0.H_kv}", "head_dim": x0.D,
               "window": x0.window, "R": x0.R, "page_size": x0.page_size,
-              "l2": "805 MB of rel_logits per call (L2 129 MB)"}
+              "l2": f"{x0.T * x0.H_q * x0.R * 4 / 1e6:.0f} MB of rel_logits per call (L2 129 MB)"}
     return dict(ms=ms, K=K, clocks=clocks, launches=4 * K, config=config, units_total=flops,
                 bytes_total=nbytes, kernel="prefill_kernel", kernel_launches=4 * K, unit="TFLOP/s")
 

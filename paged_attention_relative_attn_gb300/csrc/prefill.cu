@@ -56,7 +56,8 @@ constexpr int kBiasBufBytes = 4 * kBiasWarpBytes;    // 128 rows
 constexpr float kRescaleThreshold = 8.0f;            // log2 units: rescale O when max grows > 2^8
 
 struct PrefillParams {
-  CUtensorMap tmap_q[4];  // tokens r + 4y of q: {D, H_q, y}, box {64, 1, 32}
+  CUtensorMap tmap_q[4];    // tokens r + 4y of q: {D, H_q, y}, box {64, 1, 32}
+  CUtensorMap tmap_out[4];  // tokens r + 4y of out: {D, H_q, y}, box {64, 1, 32}, 128B swizzle
   CUtensorMap tmap_k;     // [num_pages][P][H_kv][D] bf16, box {64, 1, BH, 1}
   CUtensorMap tmap_v;
   CUtensorMap tmap_bias;  // sheared view of rel_logits: {x col, token, row-in-group}, box {68, 1, 32}
@@ -466,23 +467,31 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       const int hl = max(cl, c0), hh = min(ch, c0 + 31);
       const int dtop = pi - t.jbase;
       const bool full_vis = __all_sync(0xffffffffu, hl == c0 && hh == c0 + 31);
-      const bool clamp = __any_sync(0xffffffffu, valid && hl <= hh && dtop - hl >= R - 1);
-      const int off = (pos0 + lg - t.jbase - 63) & 3;
-      const float* half_band = my_half0 + buf * (kBiasBufBytes / 4);
       float s[32];
-      switch (off) {
-        case 0: half_scores<0>(s, sraw, half_band, scale); break;
-        case 1: half_scores<1>(s, sraw, half_band, scale); break;
-        case 2: half_scores<2>(s, sraw, half_band, scale); break;
-        default: half_scores<3>(s, sraw, half_band, scale); break;
+      if (pos0 - t.jbase - 63 >= R) {
+        // every distance of the tile is past the table (row 0 is the nearest):
+        // all of them take its last column, and no band was loaded
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) s[cc] = fmaf(__uint_as_float(sraw[cc]), scale, clampv);
+      } else {
+        const int off = (pos0 + lg - t.jbase - 63) & 3;
+        const float* half_band = my_half0 + buf * (kBiasBufBytes / 4);
+        switch (off) {
+          case 0: half_scores<0>(s, sraw, half_band, scale); break;
+          case 1: half_scores<1>(s, sraw, half_band, scale); break;
+          case 2: half_scores<2>(s, sraw, half_band, scale); break;
+          default: half_scores<3>(s, sraw, half_band, scale); break;
+        }
+        if (__any_sync(0xffffffffu, valid && hl <= hh && dtop - hl >= R)) {
+          // distances past the table take its last column (the band holds
+          // other values there)
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc)
+            if (dtop - (c0 + cc) >= R) s[cc] = fmaf(__uint_as_float(sraw[cc]), scale, clampv);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&b_empty[buf]));  // band read: the loader may refill it
-      if (clamp) {  // distances >= R - 1 share the table's last column
-#pragma unroll
-        for (int cc = 0; cc < 32; ++cc)
-          if (dtop - (c0 + cc) >= R - 1) s[cc] = fmaf(__uint_as_float(sraw[cc]), scale, clampv);
-      }
       if (!full_vis) {
 #pragma unroll
         for (int cc = 0; cc < 32; ++cc) s[cc] = (c0 + cc >= cl && c0 + cc <= ch) ? s[cc] : -INFINITY;
@@ -598,6 +607,12 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       const float inv = L > 0.f ? 1.f / L : 0.f;
       sc_a *= inv;
       sc_b *= inv;
+      // A full tile (D = 128) leaves through shared memory -- the Q buffer,
+      // free now that every MMA has completed -- and one TMA store per warp
+      // (its 32 rows x D/2 columns); rows of a partial tile past the sequence
+      // belong to the next one, so those tiles are stored row by row.
+      const bool via_smem = D == 128 && nrows == kQRows;
+      uint8_t* stage = smem + (grp * 4 + lg) * 4096;  // 32 rows x 128 B, 128B-swizzled
       __nv_bfloat16* orow = p.out + ((size_t)(t0 + i) * p.H_q + h) * D + (D / 2) * grp;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -605,18 +620,36 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
         tmem_ld32(tlane + kOCol + (D / 2) * grp + 32 * cc, oa);
         tmem_ld32(tlane + kOCol + kOHalfStride + (D / 2) * grp + 32 * cc, ob);
         tmem_ld_wait();
-        if (valid) {
-          uint32_t pkd[16];
+        uint32_t pkd[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
-            pkd[x] = pack_bf16(
-                fmaf(__uint_as_float(oa[2 * x]), sc_a, __uint_as_float(ob[2 * x]) * sc_b),
-                fmaf(__uint_as_float(oa[2 * x + 1]), sc_a, __uint_as_float(ob[2 * x + 1]) * sc_b));
+        for (int x = 0; x < 16; ++x)
+          pkd[x] = pack_bf16(
+              fmaf(__uint_as_float(oa[2 * x]), sc_a, __uint_as_float(ob[2 * x]) * sc_b),
+              fmaf(__uint_as_float(oa[2 * x + 1]), sc_a, __uint_as_float(ob[2 * x + 1]) * sc_b));
+        if (via_smem) {
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {  // 16-byte chunk 4cc + x of my 128-byte row
+            const int c = 4 * cc + x;
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
+          }
+        } else if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
 #pragma unroll
           for (int x = 0; x < 4; ++x)
             dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
         }
+      }
+      if (via_smem) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int tok = t0 + lg;  // rows lg + 4y = tokens tok + 4y
+          tma_store_3d(&p.tmap_out[tok & 3], smem_u32(stage), (D / 2) * grp, h, tok >> 2);
+          bulk_commit_group();
+          bulk_wait_group0();  // complete before the CTA (and its shared memory) ends
+        }
+        __syncwarp();
       }
       if (valid && grp == 0 && p.lse_out)
         p.lse_out[(size_t)(t0 + i) * p.H_q + h] = L > 0.f ? M + log2f(L) * kLn2 : -INFINITY;
@@ -658,9 +691,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       }
       const uint32_t fb = smem_u32(&b_full[buf]);
       const uint32_t buf_smem = band_smem + buf * kBiasBufBytes;
+      // a tile whose every distance is past the table needs no band
+      const bool beyond = pos0 - t.jbase - 63 >= R;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // row group j: rows j + 4y = tokens t0 + j + 4y
-        if (j >= nrows) continue;
+        if (j >= nrows || beyond) continue;
         const int tf = t0 + j;
         const int lo4_0 = (pos0 + j - t.jbase - 63) & ~3;
         // the map's bounds are checked on the sheared x: a negative x would
@@ -744,6 +779,17 @@ int launch_prefill(const PrefillCall& c) {
     const char* base = static_cast<const char*>(c.q) + (c.T > r ? r : 0) * tok_bytes;
     if (!encode_tiled(&prm.tmap_q[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<char*>(base),
                       dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return INKLING_ERR_CUDA;
+  }
+  for (int r = 0; r < 4; ++r) {  // out, same row split as q (D = 128 only)
+    if (c.D != 128) break;
+    const uint64_t rows = c.T > r ? (uint64_t)(c.T - r + 3) / 4 : 1;
+    uint64_t dims[3] = {(uint64_t)c.D, (uint64_t)c.H_q, rows};
+    uint64_t strides[2] = {(uint64_t)c.D * 2, 4 * tok_bytes};
+    uint32_t box[3] = {64, 1, 32};
+    char* base = static_cast<char*>(c.out) + (c.T > r ? r : 0) * tok_bytes;
+    if (!encode_tiled(&prm.tmap_out[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides,
+                      box, CU_TENSOR_MAP_SWIZZLE_128B))
       return INKLING_ERR_CUDA;
   }
   {

@@ -353,15 +353,17 @@ CHUNKED_PREFILL = dict(n_seqs=4, seq_len=8192, chunk=2048, H_q=48, H_kv=16,
                        D=128, P=64, window=512, R=512)
 
 
-def make_chunked_prefill(chunk_index, *, device="cpu", seed=0, cache=None):
+def make_chunked_prefill(chunk_index, *, device="cpu", seed=0, cache=None, n_seqs=None):
     """Call ``chunk_index`` (0..3) of the chunked-prefill workload: every
-    sequence processes tokens [2048*c, 2048*(c+1)) against the cached prefix."""
+    sequence processes tokens [2048*c, 2048*(c+1)) against the cached prefix.
+    ``n_seqs`` keeps only that many sequences (a smaller case of the same shape)."""
     c = CHUNKED_PREFILL
+    n = c["n_seqs"] if n_seqs is None else int(n_seqs)
     if cache is None:
-        cache = make_prefill_cache([c["seq_len"]] * c["n_seqs"], c["H_kv"], c["D"],
+        cache = make_prefill_cache([c["seq_len"]] * n, c["H_kv"], c["D"],
                                    c["P"], device=device, seed=seed)
-    q_lens = [c["chunk"]] * c["n_seqs"]
-    kv_lens = [c["chunk"] * (chunk_index + 1)] * c["n_seqs"]
+    q_lens = [c["chunk"]] * n
+    kv_lens = [c["chunk"] * (chunk_index + 1)] * n
     return make_prefill(cache, q_lens, kv_lens, c["H_q"], c["R"], c["window"],
                         device=device, seed=seed + 100 * (chunk_index + 1),
                         max_seq_len=c["seq_len"],
