@@ -6,30 +6,35 @@
 // applying the relative bias to the scores; "Architecture": bias per (query
 // token, head, relative distance), sliding window 512 / full causal).
 //
-// One CTA per (128-query tile of one sequence, query head), 6 warps:
-//  * warp 0 loads the Q tile once (TMA) and walks the tile's visible key range
-//    in page-respecting tiles of 64 keys (TMA of K and V, 128-byte swizzle,
-//    2-stage ring), exactly like the decode kernel;
+// One CTA per (128-query tile of one sequence, query head), 12 warps:
+//  * warp 0 loads the Q tile once (TMA) and then the K tiles of the tile's
+//    visible key range into a 3-stage ring, in page-respecting tiles of 64
+//    keys exactly like the decode kernel; warp 6 loads the V tiles the same
+//    way into a 2-stage ring (128-byte swizzle);
+//  * warp 7 loads the bias bands (below) into a 3-buffer ring;
 //  * warp 1 owns tensor memory (S double buffer 2 x 64 columns, and two O
-//    accumulators of D columns, one per half of the key columns)
-//    and one of its threads issues the MMAs: S_k = Q K_k^T (A and B from shared
-//    memory, K-major) and O += P_{k-1} V_{k-1} (A = P from tensor memory, B = V
+//    accumulators of D columns, one per half of the key columns) and one of
+//    its threads issues the MMAs: S_k = Q K_k^T (A and B from shared memory,
+//    K-major) and O += P_{k-1} V_{k-1} (A = P from tensor memory, B = V
 //    MN-major from shared memory), so QK^T of tile k overlaps the softmax of
 //    tile k-1;
-//  * warps 2-5 and 8-11 are two softmax warpgroups: a thread owns one query
-//    row (one TMEM lane) and one half of the key columns of each tile.  They read S with tcgen05.ld, add the bias, apply the causal /
-//    window mask, keep the running max lazily (O is rescaled in tensor memory
-//    only when the max grows by more than 2^8), write P (bf16) back into the S
-//    columns with tcgen05.st, and finally normalise O and store it.
+//  * warps 2-5 and 8-11 are two softmax warpgroups sharing every row: a
+//    thread owns one query row (one TMEM lane) and one half of the key
+//    columns of each tile.  It reads S with tcgen05.ld, adds the bias, applies
+//    the causal / window mask, keeps its half's running max lazily (its O is
+//    rescaled in tensor memory only when the max grows by more than 2^8) and
+//    writes P (bf16) back over its S columns with tcgen05.st; the epilogue
+//    merges the two halves and stores the normalised output (full tiles
+//    through shared memory and TMA).
 //
-// The bias (the dominant HBM stream: every query row reads its own band of
-// rel_logits, 64 distances per key tile, each element exactly once) is
-// prefetched two tiles ahead by the softmax warps with 16-byte cp.async into
-// per-row shared-memory bands.  Rows are assigned to TMEM lanes interleaved by
-// four (lane y of lane group j holds query row j + 4y; Q is loaded in that row
-// order by four TMA maps, one per token residue mod 4), so that within a warp
-// every row's band has the same alignment and is read with conflict-free
-// 16-byte shared loads.
+// The bias is the dominant HBM stream: every query row reads its own band of
+// rel_logits, 64 distances per key tile, each element exactly once.  Rows are
+// assigned to TMEM lanes interleaved by four (lane y of lane group j holds
+// query row j + 4y; Q is loaded in that row order by four TMA maps, one per
+// token residue mod 4), so that within a group of 32 rows the band start
+// moves by exactly 4 floats per row: one box of a sheared 3-D view of
+// rel_logits loads a whole group, and every row's band has the same alignment
+// and is read with conflict-free 16-byte shared loads.
 #include <cuda_bf16.h>
 #include <math.h>
 

@@ -27,12 +27,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Copy 128 rows x 32 bytes of a shared-memory matrix (described like an MMA
-// operand) into tensor memory: row r -> lane r, 8 columns from `taddr`.
-// Ordered before later tcgen05.mma of the same thread.
-__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
-}
 // Arrive (count 1) on `bar` once every tcgen05.mma issued so far by this
 // thread has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
