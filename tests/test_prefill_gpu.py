@@ -102,6 +102,22 @@ def test_chunked_prefill_full_size_sampled(ops, chunk):
     assert_close(out.index_select(0, idx), ro, lse.index_select(0, idx), rl, what="chunked")
 
 
+@pytest.mark.parametrize("chunk", [1, 3])
+def test_global_prefill_full_size_sampled(ops, chunk):
+    """The global-layer chunked prefill (4 x 2048 query tokens against the
+    cached prefix, 8 KV heads, full causal, R = 1024: most distances are past
+    the table) at full size, on sampled rows: tile edges, rows whose nearest
+    keys cross distance R - 1, and the last row."""
+    inp, _ = W.make_chunked_prefill(chunk, device=DEV, seed=0, cfg=W.GLOBAL_PREFILL)
+    out, lse = run(ops, inp)
+    assert torch.isfinite(out.float()).all()
+    rows = {0: [0, 127, 128, 1023, 1024, 2047], 2: [1, 1000], 3: [2046, 2047]}
+    ro, rl, toks = oracle_rows(inp, rows)
+    idx = torch.tensor(toks, device=DEV)
+    assert_close(out.index_select(0, idx), ro, lse.index_select(0, idx), rl,
+                 what=f"global prefill call {chunk}")
+
+
 def test_global_layer_prefill_sampled(ops):
     """A global-layer prefill (full causal, R=1024, distances clamped)."""
     kv = [3000, 1500]

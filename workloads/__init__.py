@@ -351,13 +351,18 @@ def make_prefill(cache: PrefillCache, q_lens, kv_lens, H_q, R, window, *,
 
 CHUNKED_PREFILL = dict(n_seqs=4, seq_len=8192, chunk=2048, H_q=48, H_kv=16,
                        D=128, P=64, window=512, R=512)
+# the same chunked prefill on a global layer: 8 KV heads, full causal, R = 1024
+GLOBAL_PREFILL = dict(n_seqs=4, seq_len=8192, chunk=2048, H_q=48, H_kv=8,
+                      D=128, P=64, window=0, R=1024)
 
 
-def make_chunked_prefill(chunk_index, *, device="cpu", seed=0, cache=None, n_seqs=None):
-    """Call ``chunk_index`` (0..3) of the chunked-prefill workload: every
-    sequence processes tokens [2048*c, 2048*(c+1)) against the cached prefix.
-    ``n_seqs`` keeps only that many sequences (a smaller case of the same shape)."""
-    c = CHUNKED_PREFILL
+def make_chunked_prefill(chunk_index, *, device="cpu", seed=0, cache=None, n_seqs=None,
+                         cfg=None):
+    """Call ``chunk_index`` (0..3) of a chunked-prefill workload (default the
+    local-layer one): every sequence processes tokens [2048*c, 2048*(c+1))
+    against the cached prefix.  ``n_seqs`` keeps only that many sequences (a
+    smaller case of the same shape)."""
+    c = CHUNKED_PREFILL if cfg is None else cfg
     n = c["n_seqs"] if n_seqs is None else int(n_seqs)
     if cache is None:
         cache = make_prefill_cache([c["seq_len"]] * n, c["H_kv"], c["D"],
