@@ -42,7 +42,9 @@ of them (monkeypatching) and check that the pins catch it.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, textbook SDPA, shift invariance, single key,
-one-hot bias, window immunity, page permutation, clamp expansion).
+one-hot bias, window immunity, page permutation, clamp expansion; for the KV
+append a hand-worked example and a read-back through the pinned gather of
+values that encode each token's position).
 """
 
 from __future__ import annotations
@@ -59,6 +61,9 @@ __all__ = [
     "attend_sequence",
     "ref_prefill",
     "ref_decode",
+    "token_positions",
+    "cache_slot",
+    "ref_kv_append",
 ]
 
 
@@ -220,3 +225,56 @@ def ref_decode(q, k_cache, v_cache, page_table, seq_lens, rel_logits,
         out[b] = o[0]
         lse[b] = l[0]
     return out, lse
+
+
+# --------------------------------------------------------------------------
+# KV append
+# --------------------------------------------------------------------------
+
+def token_positions(cu_seqlens_q, seq_lens) -> np.ndarray:
+    """Absolute position of every packed token: token i of sequence b (packed
+    index ``cu_seqlens_q[b] + i``) is one of the LAST ``q_len_b`` tokens of a
+    sequence of ``seq_lens[b]`` tokens, so it sits at ``seq_lens[b] - q_len_b + i``
+    (decode: one token per sequence, at ``seq_lens[b] - 1``)."""
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    sl = np.asarray(seq_lens, dtype=np.int64)
+    pos = np.zeros(int(cu[-1]), dtype=np.int64)
+    for b in range(len(sl)):
+        n = int(cu[b + 1] - cu[b])
+        for i in range(n):
+            pos[int(cu[b]) + i] = int(sl[b]) - n + i
+    return pos
+
+
+def cache_slot(page_row, p: int, P: int):
+    """Physical (page, slot) of logical token ``p`` of a sequence whose page
+    table row is ``page_row`` (vLLM PR #51560, "Purpose": attention always runs
+    over the paged cache; token p lives in page ``p // P`` of the sequence)."""
+    return int(page_row[p // P]), p % P
+
+
+def ref_kv_append(k_cache, v_cache, page_table, cu_seqlens_q, seq_lens, k_new, v_new):
+    """Write the new tokens' K/V into the paged cache (TensorRT-LLM PR #17062,
+    commit notes: the attention op itself writes the step's K/V into the cache
+    before reading it, hence ``skip_kv_write`` for the backend; vLLM PR #51560,
+    "Purpose": the cache is paged through ``page_table``).
+
+    Token t of sequence b at position p (``token_positions``) goes to physical
+    page ``page_table[b, p // P]``, slot ``p % P``: all H_kv heads of its K row
+    and of its V row.  Every other slot is left as it was.
+
+    k/v_cache [num_pages, P, H_kv, D]; k/v_new [T, H_kv, D].  Returns new
+    arrays (the inputs are not modified).
+    """
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    pt = np.asarray(page_table, dtype=np.int64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    P = kc.shape[1]
+    pos = token_positions(cu_seqlens_q, seq_lens)
+    for b in range(len(cu) - 1):
+        for t in range(int(cu[b]), int(cu[b + 1])):
+            page, slot = cache_slot(pt[b], int(pos[t]), P)
+            kc[page, slot] = k_new[t]
+            vc[page, slot] = v_new[t]
+    return kc, vc

@@ -307,11 +307,58 @@ def pin_empty_sequence(R=ref):
     assert np.isfinite(lse[1]).all()
 
 
+def pin_kv_append_hand(R=ref):
+    """Worked by hand: P = 4, the sequence's pages are [2, 0], 6 tokens in
+    total of which the last 3 are appended: positions 3, 4, 5 land in
+    (page 2, slot 3), (page 0, slot 0), (page 0, slot 1)."""
+    kc = np.zeros((3, 4, 1, 1))
+    vc = np.zeros((3, 4, 1, 1))
+    k_new = np.array([10.0, 20.0, 30.0]).reshape(3, 1, 1)
+    v_new = -k_new
+    k2, v2 = R.ref_kv_append(kc, vc, np.array([[2, 0]]), np.array([0, 3]), np.array([6]),
+                             k_new, v_new)
+    expect = np.zeros((3, 4, 1, 1))
+    expect[2, 3] = 10.0
+    expect[0, 0] = 20.0
+    expect[0, 1] = 30.0
+    assert np.array_equal(k2, expect) and np.array_equal(v2, -expect)
+    assert np.array_equal(kc, np.zeros_like(kc))  # inputs untouched
+
+
+def pin_kv_append_readback(R=ref):
+    """Append every token of three sequences, in two chunks each, into a
+    NaN-poisoned pool laid out by the input generator's page tables; the
+    (separately pinned) gather must read back each sequence's values in
+    position order, and every slot no token owns must still be NaN."""
+    lens = [9, 1, 17]
+    P, H, D = 4, 2, 3
+    gc = torch.Generator().manual_seed(3)
+    max_pages = max(W.pages_for(L, P) for L in lens)
+    pool = sum(W.pages_for(L, P) for L in lens) + 2
+    pt, _ = W.build_page_table(lens, P, max_pages, pool, gc)
+    pt = npi(pt)
+    kc = np.full((pool, P, H, D), np.nan)
+    vc = np.full((pool, P, H, D), np.nan)
+    first = [L // 2 for L in lens]
+    for lo_of, hi_of in ((lambda b: 0, lambda b: first[b]), (lambda b: first[b], lambda b: lens[b])):
+        q_lens = [hi_of(b) - lo_of(b) for b in range(3)]
+        cu = np.concatenate([[0], np.cumsum(q_lens)])
+        vals = np.concatenate([1000.0 * b + np.arange(lo_of(b), hi_of(b)) for b in range(3)])
+        k_new = np.broadcast_to(vals[:, None, None], (len(vals), H, D)).copy()
+        kc, vc = R.ref_kv_append(kc, vc, pt, cu, [hi_of(b) for b in range(3)], k_new, -k_new)
+    for b, L in enumerate(lens):
+        got = R.gather_sequence(kc, pt[b], L)
+        want = np.broadcast_to((1000.0 * b + np.arange(L))[:, None, None], (L, H, D))
+        assert np.array_equal(got, want)
+        assert np.array_equal(R.gather_sequence(vc, pt[b], L), -want)
+    assert int(np.isnan(kc[:, :, 0, 0]).sum()) == pool * P - sum(lens)
+
+
 ALL_PINS = [pin_brute_tiny_decode, pin_brute_small_decode, pin_brute_small_prefill,
             pin_zero_bias_is_sdpa, pin_constant_bias_shift, pin_single_visible_key,
             pin_one_hot_bias, pin_window_immunity, pin_page_permutation,
             pin_clamp_expansion, pin_closed_form, pin_decode_is_last_prefill_token,
-            pin_empty_sequence]
+            pin_empty_sequence, pin_kv_append_hand, pin_kv_append_readback]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -329,6 +376,10 @@ MUTANTS = {
     "clamp_off_by_one": ("distance_index", lambda p, j, R: np.minimum(p - j, R - 2)),
     "window_off_by_one": ("visible", lambda p, j, w: (j <= p) & (((p - j) <= w) if w > 0 else True)),
     "not_causal": ("visible", lambda p, j, w: ((p - j) < w) if w > 0 else np.ones_like(j, bool)),
+    "append_position_off_by_one": ("token_positions", lambda cu, sl: (lambda c, s: np.concatenate(
+        [[int(s[b]) - int(c[b + 1] - c[b]) + i + 1 for i in range(int(c[b + 1] - c[b]))]
+         for b in range(len(s))] + [[]]).astype(np.int64))(np.asarray(cu), np.asarray(sl))),
+    "append_slot_transposed": ("cache_slot", lambda row, p, P: (int(row[p // P]), (p // P) % P)),
 }
 
 
