@@ -310,6 +310,43 @@ def bench_prefill(args, device, K, warmup, name="chunked_prefill"):
                 bound="tensor" if name == "global_prefill" else "hbm")
 
 
+def bench_kv_append(args, device, K, warmup):
+    """One step = the KV append of one chunked-prefill call: 4 sequences x 2048
+    new tokens (16 KV heads, D = 128, pages of 64) written at positions
+    2048c .. 2048c + 2047, c cycling over the four calls, so consecutive steps
+    write different cache slots from different inputs (4 x 134 MB per
+    rotation, L2 129 MB).  Bytes: every new K and V row read once and written
+    once."""
+    import paged_attention_relative_attn_gb300 as ira
+    cfg = W.CHUNKED_PREFILL
+    n = cfg["n_seqs"] if args.batch is None else args.batch
+    chunk, L = cfg["chunk"], cfg["seq_len"]
+    cache = W.make_prefill_cache([L] * n, cfg["H_kv"], cfg["D"], cfg["P"], device=device, seed=0)
+    g = torch.Generator(device=device).manual_seed(5)
+    T = n * chunk
+    cu = (torch.arange(n + 1, dtype=torch.int32) * chunk).to(device)
+    calls = []
+    for c in range(4):
+        k_new = torch.randn((T, cfg["H_kv"], cfg["D"]), generator=g, device=device).to(torch.bfloat16)
+        v_new = torch.randn((T, cfg["H_kv"], cfg["D"]), generator=g, device=device).to(torch.bfloat16)
+        sl = torch.full((n,), chunk * (c + 1), dtype=torch.int32, device=device)
+        calls.append((k_new, v_new, sl))
+    per_call = 2 * 2 * T * cfg["H_kv"] * cfg["D"] * 2
+
+    def step(i, stream):
+        k_new, v_new, sl = calls[i % 4]
+        ira.kv_append(k_new, v_new, cu, sl, cache.page_table, cache.k_cache, cache.v_cache,
+                      stream=stream)
+
+    ms, clocks = time_steps(args, device, step, K, warmup, 40)
+    config = {"workload": "kv_append", "sequences": n, "tokens_per_call": T,
+              "heads_kv": cfg["H_kv"], "head_dim": cfg["D"], "page_size": cfg["P"],
+              "l2": f"4 calls x {per_call / 1e6:.0f} MB per rotation (L2 129 MB)"}
+    return dict(ms=ms, K=K, clocks=clocks, launches=K, config=config, units_total=K * per_call,
+                bytes_total=K * per_call, kernel="kv_append_kernel", kernel_launches=K,
+                unit="GB/s")
+
+
 def bench_stack(args, device, K, warmup):
     """One step = one decode step over the 66-layer stack: 55 local layers
     (16 KV heads, window 512, R=512) and 11 global layers (8 KV heads, full
@@ -544,8 +581,10 @@ def run_reference(args):
 
 
 DEFAULT_STEPS = {"local_decode": 10000, "global_decode": 2000, "chunked_prefill": 200,
-                 "global_prefill": 50, "decode_66_layers": 40}
+                 "global_prefill": 50, "kv_append": 2000, "decode_66_layers": 40}
 KERNEL_SOURCES = {
+    "kv_append_kernel": ["paged_attention_relative_attn_gb300/csrc/kv_append.cu",
+                         "paged_attention_relative_attn_gb300/csrc/plan.cuh"],
     "decode_kernel": ["paged_attention_relative_attn_gb300/csrc/decode.cu",
                       "paged_attention_relative_attn_gb300/csrc/plan.cuh",
                       "paged_attention_relative_attn_gb300/csrc/ptx.cuh"],
@@ -561,6 +600,8 @@ def run_workload(args, device, name, K, warmup):
         return bench_decode(args, device, name, K, warmup)
     if name in PREFILL_WORKLOADS:
         return bench_prefill(args, device, K, warmup, name)
+    if name == "kv_append":
+        return bench_kv_append(args, device, K, warmup)
     return bench_stack(args, device, K, warmup)
 
 
@@ -614,7 +655,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="local_decode",
                     choices=["local_decode", "global_decode", "chunked_prefill",
-                             "global_prefill", "decode_66_layers"])
+                             "global_prefill", "kv_append", "decode_66_layers"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=5.0)
@@ -673,7 +714,7 @@ def main():
     if not args.no_extra and args.workload == "local_decode":
         extra = {}
         for name, K in (("global_decode", 1000), ("chunked_prefill", 100),
-                        ("global_prefill", 20), ("decode_66_layers", 20)):
+                        ("global_prefill", 20), ("kv_append", 1000), ("decode_66_layers", 20)):
             rr = run_workload(args, device, name, K, 5)
             extra[name] = summarize(args, rr, pk)
             del rr

@@ -167,6 +167,41 @@ int inkling_rel_attn_prefill(
     size_t workspace_bytes, int32_t* device_error, void* stream);
 
 /*
+ * inkling_rel_attn_kv_append -- write the new tokens' K and V rows into the
+ * paged cache, the step right before decode / prefill reads it (TensorRT-LLM
+ * PR #17062, commit notes: the attention op writes the step's K/V into the
+ * cache itself before reading it -- `skip_kv_write` for the backend).
+ *
+ * Token numbering is the prefill's: sequence b owns the packed tokens
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1, the LAST q_len_b of its seq_lens[b]
+ * tokens, so token i sits at position p = seq_lens[b] - q_len_b + i (decode:
+ * cu_seqlens_q = 0, 1, .., B and p = seq_lens[b] - 1).  Its K row (all H_kv
+ * heads, H_kv * D bf16, contiguous) is copied to
+ * k_cache[page_table[b * page_table_stride + p / page_size]][p % page_size],
+ * and likewise its V row.  No other byte of the cache is written.
+ *
+ *   k_new, v_new  bf16 [T, H_kv, D] (device), 16-byte aligned
+ *   k_cache, v_cache bf16 [num_pages, page_size, H_kv, D] (device), written
+ *   cu_seqlens_q  int32 [B + 1] (device), non-decreasing, [0] = 0, [B] = T
+ *   seq_lens      int32 [B] (device), total tokens incl. the appended ones
+ *   page_table    int32 [B, page_table_stride] (device)
+ * The caller owns every buffer; nothing is allocated or synchronised, and the
+ * call can be captured in a CUDA graph.  Returns INKLING_OK or a negative
+ * INKLING_ERR_* code (arguments are checked on the host before anything
+ * launches: D in {64, 128}, page_size a multiple of 16 up to 256, positive
+ * pool / stride, 16-byte alignment).  On the device a token whose chunk is
+ * inconsistent (q_len_b > seq_lens[b]) sets INKLING_DEVERR_BAD_CHUNK, one past
+ * its page-table row INKLING_DEVERR_SEQ_TOO_LONG, one whose page id is outside
+ * [0, num_pages) INKLING_DEVERR_BAD_PAGE; such tokens are not written.
+ */
+int inkling_rel_attn_kv_append(
+    const void* k_new, const void* v_new, const int32_t* cu_seqlens_q,
+    const int32_t* seq_lens, const int32_t* page_table,
+    int32_t page_table_stride, int32_t B, int32_t T, int32_t H_kv, int32_t D,
+    int32_t page_size, int32_t num_pages, void* k_cache, void* v_cache,
+    int32_t* device_error, void* stream);
+
+/*
  * inkling_rel_attn_choose_splits -- the decode split count, a pure host
  * function of host scalars (so it is identical at graph capture and replay,
  * and independent of physical page ids).  vLLM PR #51560, "Changes": the

@@ -11,9 +11,10 @@ from .ops import (  # noqa: F401
     decode,
     decode_inputs,
     decode_workspace_bytes,
+    kv_append,
     prefill,
     prefill_inputs,
 )
 
 __all__ = ["InklingError", "choose_splits", "decode", "decode_inputs", "decode_workspace_bytes",
-           "prefill", "prefill_inputs"]
+           "kv_append", "prefill", "prefill_inputs"]

@@ -19,6 +19,7 @@ EXPORTED = (
     "inkling_rel_attn_decode",
     "inkling_rel_attn_decode_noalloc",
     "inkling_rel_attn_prefill",
+    "inkling_rel_attn_kv_append",
     "inkling_rel_attn_choose_splits",
     "inkling_rel_attn_decode_workspace_size",
     "inkling_rel_attn_prefill_workspace_size",
@@ -50,6 +51,10 @@ _SIGS = {
         _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B T max_q_len H_q H_kv D page_size
         _i32, _i32, _i32, _f32, _i32,               # num_pages R window scale max_seq_len
         _p, _p, _p, _sz, _p, _p]),                  # out lse ws ws_bytes err stream
+    "inkling_rel_attn_kv_append": (ctypes.c_int, [
+        _p, _p, _p, _p, _p, _i32,                   # k_new v_new cu seq_lens page_table stride
+        _i32, _i32, _i32, _i32, _i32, _i32,         # B T H_kv D page_size num_pages
+        _p, _p, _p, _p]),                           # k_cache v_cache err stream
     "inkling_rel_attn_choose_splits": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "inkling_rel_attn_decode_workspace_size": (_sz, [_i32] * 8),
     "inkling_rel_attn_prefill_workspace_size": (_sz, [_i32] * 3),
@@ -112,6 +117,15 @@ def inkling_rel_attn_prefill(q, cu_seqlens_q, k_cache, v_cache, page_table, page
         _v(seq_lens), _v(rel_logits), B, T, max_q_len, H_q, H_kv, D, page_size, num_pages, R,
         window, scale, max_seq_len, _v(out), _v(lse_out), _v(workspace), workspace_bytes,
         _v(device_error), _v(stream))
+
+
+def inkling_rel_attn_kv_append(k_new, v_new, cu_seqlens_q, seq_lens, page_table,
+                               page_table_stride, B, T, H_kv, D, page_size, num_pages, k_cache,
+                               v_cache, device_error, stream):
+    return load().inkling_rel_attn_kv_append(
+        _v(k_new), _v(v_new), _v(cu_seqlens_q), _v(seq_lens), _v(page_table), page_table_stride,
+        B, T, H_kv, D, page_size, num_pages, _v(k_cache), _v(v_cache), _v(device_error),
+        _v(stream))
 
 
 def inkling_rel_attn_choose_splits(B, H_kv, window, max_seq_len, num_sms):

@@ -51,8 +51,23 @@ struct PrefillCall {
   cudaStream_t stream;
 };
 
-int launch_decode(const DecodeCall& c);    // returns INKLING_* code
-int launch_prefill(const PrefillCall& c);  // returns INKLING_* code
+struct KvAppendCall {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  int32_t pt_stride;
+  int32_t B, T, H_kv, D, P, num_pages;
+  void* k_cache;
+  void* v_cache;
+  int32_t* dev_err;
+  cudaStream_t stream;
+};
+
+int launch_decode(const DecodeCall& c);        // returns INKLING_* code
+int launch_prefill(const PrefillCall& c);      // returns INKLING_* code
+int launch_kv_append(const KvAppendCall& c);   // returns INKLING_* code
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,

@@ -125,6 +125,35 @@ def prefill(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens, rel_logits,
     return out, lse
 
 
+def kv_append(k_new, v_new, cu_seqlens_q, seq_lens, page_table, k_cache, v_cache, *,
+              device_error=None, stream=None):
+    """Write the new tokens' K/V into the paged cache (in place).  See
+    inkling_rel_attn_kv_append.
+
+    k_new, v_new [T, H_kv, D] bf16; cu_seqlens_q [B+1] int32; seq_lens [B]
+    int32 (totals including the new tokens); page_table [B, stride] int32;
+    k_cache, v_cache [num_pages, page_size, H_kv, D] bf16, updated in place.
+    """
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    T, H_kv, D = k_new.shape
+    num_pages, P, H_kv_c, D_c = k_cache.shape
+    B = seq_lens.shape[0]
+    if (v_new.shape != k_new.shape or v_cache.shape != k_cache.shape or (H_kv_c, D_c) != (H_kv, D)
+            or cu_seqlens_q.shape[0] != B + 1 or page_table.shape[0] != B):
+        raise ValueError("inconsistent shapes")
+    rc = _lib.inkling_rel_attn_kv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(page_table),
+        page_table.shape[1], B, T, H_kv, D, P, num_pages, _ptr(k_cache), _ptr(v_cache),
+        _ptr(device_error), _stream(k_new.device, stream))
+    _check(rc, "inkling_rel_attn_kv_append")
+
+
 def decode_inputs(inp, **kw):
     """``decode`` on a workloads.DecodeInputs-like object."""
     return decode(inp.q, inp.k_cache, inp.v_cache, inp.page_table, inp.seq_lens, inp.rel_logits,

@@ -115,3 +115,20 @@ def test_prefill_argument_validation(lib):
     assert lib.inkling_rel_attn_prefill(**{**a, "R": 30}) == -1
     assert lib.inkling_rel_attn_prefill(**{**a, "rel_logits": 8}) == -2
     assert lib.inkling_rel_attn_prefill(**{**a, "T": 0}) == 0
+
+
+def test_kv_append_argument_validation(lib):
+    a = dict(k_new=16, v_new=16, cu_seqlens_q=4, seq_lens=4, page_table=4, page_table_stride=4,
+             B=2, T=2, H_kv=2, D=64, page_size=16, num_pages=8, k_cache=16, v_cache=16,
+             device_error=None, stream=None)
+    rc = lambda **o: lib.inkling_rel_attn_kv_append(**{**a, **o})  # noqa: E731
+    assert rc(D=96) == -1
+    assert rc(page_size=24) == -1
+    assert rc(num_pages=0) == -1
+    assert rc(H_kv=0) == -1
+    assert rc(B=-1) == -1
+    assert rc(T=0) == 0                 # nothing to write
+    assert rc(B=0) == 0
+    assert rc(k_new=None) == -1
+    assert rc(k_cache=24) == -2         # 16-byte alignment
+    assert rc(seq_lens=6) == -2
