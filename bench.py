@@ -310,6 +310,79 @@ def bench_prefill(args, device, K, warmup, name="chunked_prefill"):
                 bound="tensor" if name == "global_prefill" else "hbm")
 
 
+MTP_DECODE = dict(B=64, q_len=4, H_q=48, H_kv=16, D=128, P=64, window=512, R=512,
+                  len_range=(1024, 8192))
+
+
+def bench_decode_multi(args, device, K, warmup):
+    """One step = one multi-token decode call on a local layer: 64 sequences
+    x 4 new tokens (3 draft tokens + 1), lengths uniform in [1024, 8192], window
+    512, R = 512.  Metric: K/V bytes of each (sequence, KV head)'s visible keys
+    -- the union over its 4 tokens, min(L, 512 + 3) keys, read once -- per
+    second.  Input sets rotate until one rotation's visible K/V exceeds 2 x L2."""
+    import paged_attention_relative_attn_gb300 as ira
+    c = MTP_DECODE
+    B = c["B"] if args.batch is None else args.batch
+    sets = []
+    while True:
+        lens = W.draw_uniform_lengths(c["B"], *c["len_range"], len(sets))[:B]
+        cache = W.make_prefill_cache(lens, c["H_kv"], c["D"], c["P"], device=device,
+                                     seed=len(sets))
+        sets.append(W.make_prefill(cache, [c["q_len"]] * B, lens, c["H_q"], c["R"], c["window"],
+                                   device=device, seed=len(sets) + 1,
+                                   max_seq_len=c["len_range"][1]))
+        kv_rot = sum(multi_decode_bytes(x, c["q_len"])[0] for x in sets)
+        if args.sets is not None:
+            if len(sets) >= args.sets:
+                break
+        elif len(sets) >= 3 and kv_rot > 2 * L2_BYTES:
+            break
+    n = len(sets)
+    per = [multi_decode_bytes(x, c["q_len"]) for x in sets]
+    x0 = sets[0]
+    ws_bytes = ira.decode_multi_workspace_bytes(B, c["q_len"], c["H_q"], c["H_kv"], c["D"],
+                                                c["window"], x0.max_seq_len)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    outs = [torch.empty_like(x.q) for x in sets]
+    lses = [torch.empty(x.q.shape[:2], dtype=torch.float32, device=device) for x in sets]
+
+    def step(i, stream):
+        x = sets[i % n]
+        ira.decode_multi(x.q, x.k_cache, x.v_cache, x.page_table, x.seq_lens, x.rel_logits,
+                         q_len=c["q_len"], window=x.window, scale=x.scale,
+                         max_seq_len=x.max_seq_len, out=outs[i % n], lse=lses[i % n],
+                         workspace=ws, stream=stream)
+
+    ms, clocks = time_steps(args, device, step, K, warmup, 60 * n // math.gcd(60, n))
+    config = {"workload": "mtp_decode", "batch": B, "q_len": c["q_len"],
+              "heads": f"{c['H_q']}/{c['H_kv']}", "head_dim": c["D"], "page_size": c["P"],
+              "window": c["window"], "R": c["R"],
+              "l2": f"rotating {n} input sets, {sum(p[0] for p in per) / 1e6:.0f} MB of visible "
+                    f"K/V per rotation (L2 129 MB)"}
+    return dict(ms=ms, K=K, clocks=clocks, launches=K, config=config,
+                units_total=sum(per[i % n][0] for i in range(K)),
+                bytes_total=sum(per[i % n][1] for i in range(K)), kernel="decode_kernel",
+                kernel_launches=K, unit="GB/s")
+
+
+def multi_decode_bytes(inp, q_len):
+    """(visible K/V bytes, all algorithmic bytes) of one multi-token decode
+    call: per (sequence, KV head) the union of its tokens' visible keys (read
+    once), plus q, out, lse and the bias entries of every row's visible keys."""
+    L = inp.seq_lens.cpu().long()
+    W_ = inp.window
+    keys = torch.clamp(L, max=W_ + q_len - 1) if W_ > 0 else L
+    kv = int(keys.sum()) * inp.H_kv * inp.D * 2 * 2
+    T = inp.T
+    q_out = T * inp.H_q * inp.D * 2 * 2
+    bias = 0
+    for i in range(q_len):
+        vis = L - q_len + i + 1
+        vis = torch.clamp(vis, max=W_) if W_ > 0 else vis
+        bias += int(torch.clamp(vis, max=inp.R).sum()) * inp.H_q * 4
+    return kv, kv + q_out + bias + T * inp.H_q * 4
+
+
 def bench_kv_append(args, device, K, warmup):
     """One step = the KV append of one chunked-prefill call: 4 sequences x 2048
     new tokens (16 KV heads, D = 128, pages of 64) written at positions
@@ -581,7 +654,8 @@ def run_reference(args):
 
 
 DEFAULT_STEPS = {"local_decode": 10000, "global_decode": 2000, "chunked_prefill": 200,
-                 "global_prefill": 50, "kv_append": 2000, "decode_66_layers": 40}
+                 "global_prefill": 50, "kv_append": 2000, "mtp_decode": 5000,
+                 "decode_66_layers": 40}
 KERNEL_SOURCES = {
     "kv_append_kernel": ["paged_attention_relative_attn_gb300/csrc/kv_append.cu",
                          "paged_attention_relative_attn_gb300/csrc/plan.cuh"],
@@ -602,6 +676,8 @@ def run_workload(args, device, name, K, warmup):
         return bench_prefill(args, device, K, warmup, name)
     if name == "kv_append":
         return bench_kv_append(args, device, K, warmup)
+    if name == "mtp_decode":
+        return bench_decode_multi(args, device, K, warmup)
     return bench_stack(args, device, K, warmup)
 
 
@@ -655,7 +731,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="local_decode",
                     choices=["local_decode", "global_decode", "chunked_prefill",
-                             "global_prefill", "kv_append", "decode_66_layers"])
+                             "global_prefill", "kv_append", "mtp_decode", "decode_66_layers"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=5.0)
@@ -714,7 +790,8 @@ def main():
     if not args.no_extra and args.workload == "local_decode":
         extra = {}
         for name, K in (("global_decode", 1000), ("chunked_prefill", 100),
-                        ("global_prefill", 20), ("kv_append", 1000), ("decode_66_layers", 20)):
+                        ("global_prefill", 20), ("kv_append", 1000), ("mtp_decode", 2000),
+                        ("decode_66_layers", 20)):
             rr = run_workload(args, device, name, K, 5)
             extra[name] = summarize(args, rr, pk)
             del rr

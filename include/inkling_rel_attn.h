@@ -138,6 +138,48 @@ int inkling_rel_attn_decode_noalloc(
     int32_t* device_error, void* stream);
 
 /*
+ * inkling_rel_attn_decode_multi -- decode of q_len >= 1 new tokens per
+ * sequence (multi-token prediction / speculative verification: the model's
+ * draft layers share the attention, TensorRT-LLM PR #17062, "Architecture").
+ *
+ * Sequence b's q_len query tokens are its LAST q_len tokens (their K/V already
+ * in the cache): token i sits at position p = seq_lens[b] - q_len + i and sees
+ * keys j <= p (and p - j < window when window > 0), with the bias
+ * rel_logits[b * q_len + i, h, min(p - j, R - 1)].  The result equals
+ * inkling_rel_attn_prefill with q_len tokens per sequence; the K/V of a
+ * (sequence, KV head) is read once per group of tokens (groups of
+ * min(q_len, 16 / G) tokens, G = H_q / H_kv), not once per token.
+ *
+ *   q          bf16 [B * q_len, H_q, D] (token-major: row b * q_len + i)
+ *   rel_logits fp32 [B * q_len, H_q, R]
+ *   out        bf16 [B * q_len, H_q, D]; lse_out fp32 [B * q_len, H_q] or NULL
+ *   q_len      1 .. 64 (1 is inkling_rel_attn_decode); seq_lens[b] >= q_len
+ *   workspace  inkling_rel_attn_decode_multi_workspace_size bytes when the
+ *              call splits the keys, else may be NULL
+ * Other arguments, ownership, errors and graph safety as for decode.  A
+ * sequence shorter than q_len sets INKLING_DEVERR_BAD_CHUNK and gets out = 0,
+ * lse = -inf.
+ */
+int inkling_rel_attn_decode_multi(
+    const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* page_table, int32_t page_table_stride,
+    const int32_t* seq_lens, const float* rel_logits, int32_t B, int32_t q_len,
+    int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages,
+    int32_t R, int32_t window, float scale, int32_t max_seq_len, void* out,
+    float* lse_out, void* workspace, size_t workspace_bytes,
+    int32_t num_splits, int32_t* device_error, void* stream);
+
+/* Workspace bytes of inkling_rel_attn_decode_multi for these scalars (0 when
+ * the call does not split the keys).  Host only; num_sms as for
+ * inkling_rel_attn_decode_workspace_size. */
+size_t inkling_rel_attn_decode_multi_workspace_size(int32_t B, int32_t q_len,
+                                                    int32_t H_q, int32_t H_kv,
+                                                    int32_t D, int32_t window,
+                                                    int32_t max_seq_len,
+                                                    int32_t num_splits,
+                                                    int32_t num_sms);
+
+/*
  * inkling_rel_attn_prefill -- chunked / paged prefill (TensorRT-LLM PR #17062,
  * "Implementation": paged prefill over the cache).
  *

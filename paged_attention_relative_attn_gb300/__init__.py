@@ -10,11 +10,14 @@ from .ops import (  # noqa: F401
     choose_splits,
     decode,
     decode_inputs,
+    decode_multi,
+    decode_multi_workspace_bytes,
     decode_workspace_bytes,
     kv_append,
     prefill,
     prefill_inputs,
 )
 
-__all__ = ["InklingError", "choose_splits", "decode", "decode_inputs", "decode_workspace_bytes",
+__all__ = ["InklingError", "choose_splits", "decode", "decode_inputs", "decode_multi",
+           "decode_multi_workspace_bytes", "decode_workspace_bytes",
            "kv_append", "prefill", "prefill_inputs"]

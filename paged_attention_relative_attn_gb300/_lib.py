@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libinkling_rel_attn.so")
 EXPORTED = (
     "inkling_rel_attn_decode",
     "inkling_rel_attn_decode_noalloc",
+    "inkling_rel_attn_decode_multi",
+    "inkling_rel_attn_decode_multi_workspace_size",
     "inkling_rel_attn_prefill",
     "inkling_rel_attn_kv_append",
     "inkling_rel_attn_choose_splits",
@@ -46,6 +48,12 @@ _SIGS = {
         _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B H_q H_kv D page_size num_pages R
         _i32, _f32, _i32,                           # window scale max_seq_len
         _p, _p, _i32, _p, _p]),                     # out lse splits err stream
+    "inkling_rel_attn_decode_multi": (ctypes.c_int, [
+        _p, _p, _p, _p, _i32, _p, _p,               # q k v page_table stride seq_lens rel
+        _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B q_len H_q H_kv D page_size num_pages
+        _i32, _i32, _f32, _i32,                     # R window scale max_seq_len
+        _p, _p, _p, _sz, _i32, _p, _p]),            # out lse ws ws_bytes splits err stream
+    "inkling_rel_attn_decode_multi_workspace_size": (_sz, [_i32] * 9),
     "inkling_rel_attn_prefill": (ctypes.c_int, [
         _p, _p, _p, _p, _p, _i32, _p, _p,           # q cu k v page_table stride seq_lens rel
         _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B T max_q_len H_q H_kv D page_size
@@ -106,6 +114,23 @@ def inkling_rel_attn_decode_noalloc(q, k_cache, v_cache, page_table, page_table_
         _v(q), _v(k_cache), _v(v_cache), _v(page_table), page_table_stride, _v(seq_lens),
         _v(rel_logits), B, H_q, H_kv, D, page_size, num_pages, R, window, scale, max_seq_len,
         _v(out), _v(lse_out), num_splits, _v(device_error), _v(stream))
+
+
+def inkling_rel_attn_decode_multi(q, k_cache, v_cache, page_table, page_table_stride, seq_lens,
+                                  rel_logits, B, q_len, H_q, H_kv, D, page_size, num_pages, R,
+                                  window, scale, max_seq_len, out, lse_out, workspace,
+                                  workspace_bytes, num_splits, device_error, stream):
+    return load().inkling_rel_attn_decode_multi(
+        _v(q), _v(k_cache), _v(v_cache), _v(page_table), page_table_stride, _v(seq_lens),
+        _v(rel_logits), B, q_len, H_q, H_kv, D, page_size, num_pages, R, window, scale,
+        max_seq_len, _v(out), _v(lse_out), _v(workspace), workspace_bytes, num_splits,
+        _v(device_error), _v(stream))
+
+
+def inkling_rel_attn_decode_multi_workspace_size(B, q_len, H_q, H_kv, D, window, max_seq_len,
+                                                 num_splits, num_sms):
+    return load().inkling_rel_attn_decode_multi_workspace_size(B, q_len, H_q, H_kv, D, window,
+                                                               max_seq_len, num_splits, num_sms)
 
 
 def inkling_rel_attn_prefill(q, cu_seqlens_q, k_cache, v_cache, page_table, page_table_stride,

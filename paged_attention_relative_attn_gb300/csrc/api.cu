@@ -162,38 +162,44 @@ int32_t inkling_rel_attn_choose_splits(int32_t B, int32_t H_kv, int32_t window, 
   return S_out;
 }
 
-size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
-                                              int32_t window, int32_t max_seq_len,
-                                              int32_t num_splits, int32_t num_sms) {
-  const int32_t keys = decode_keys_max(window, max_seq_len);
+}  // extern "C"
+
+namespace ira {
+// Split plan of a (multi-token) decode call: keys per item, split count and
+// keys per split.  q_len = 1 is plain decode.
+static void decode_call_plan(int32_t B, int32_t q_len, int32_t H_q, int32_t H_kv, int32_t window,
+                             int32_t max_seq_len, int32_t num_splits, int32_t num_sms,
+                             int32_t* keys_out, int32_t* S_out, int32_t* chunk_out) {
+  const int32_t G = H_kv > 0 ? H_q / H_kv : 1;
+  const int32_t TG = decode_token_group(q_len, G);
+  const int32_t NG = (std::max(q_len, 1) + TG - 1) / TG;
+  // a group's keys: its first token's window plus the TG - 1 later positions
+  const int32_t w_eff = window > 0 ? window + TG - 1 : 0;
+  const int32_t keys = decode_keys_max(w_eff, max_seq_len);
   int32_t S_req = num_splits;
   if (S_req <= 0) {
     if (num_sms <= 0) {
       DevInfo di = device_info();
       num_sms = di.ok >= 0 && di.sms > 0 ? di.sms : 152;
     }
-    S_req = inkling_rel_attn_choose_splits(B, H_kv, window, max_seq_len, num_sms);
+    S_req = inkling_rel_attn_choose_splits(
+        (int32_t)std::min<int64_t>((int64_t)B * NG, INT32_MAX), H_kv, w_eff, max_seq_len, num_sms);
   }
-  int32_t S, chunk;
-  decode_split_plan(keys, S_req, &S, &chunk);
-  return decode_workspace_bytes(B, H_q, D, S);
+  *keys_out = keys;
+  decode_split_plan(keys, S_req, S_out, chunk_out);
 }
 
-size_t inkling_rel_attn_prefill_workspace_size(int32_t T, int32_t H_q, int32_t D) {
-  (void)T;
-  (void)H_q;
-  (void)D;
-  return 0;
-}
-
-int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                            const int32_t* page_table, int32_t page_table_stride,
-                            const int32_t* seq_lens, const float* rel_logits, int32_t B, int32_t H_q,
-                            int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, int32_t R,
-                            int32_t window, float scale, int32_t max_seq_len, void* out,
-                            float* lse_out, void* workspace, size_t workspace_bytes,
-                            int32_t num_splits, int32_t* device_error, void* stream) {
-  if (B < 0 || max_seq_len < 0) return INKLING_ERR_ARG;
+// Validated decode of q_len >= 1 query tokens per sequence.
+static int decode_call(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* page_table, int32_t page_table_stride,
+                       const int32_t* seq_lens, const float* rel_logits, int32_t B, int32_t q_len,
+                       int32_t H_q, int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages,
+                       int32_t R, int32_t window, float scale, int32_t max_seq_len, void* out,
+                       float* lse_out, void* workspace, size_t workspace_bytes,
+                       int32_t num_splits, int32_t* device_error, void* stream) {
+  if (B < 0 || max_seq_len < 0 || q_len < 1 || q_len > 64) return INKLING_ERR_ARG;
+  if (q_len > 1 && max_seq_len < q_len) return INKLING_ERR_ARG;
+  if ((int64_t)B * q_len * H_q > INT32_MAX / 4) return INKLING_ERR_ARG;
   if (!common_shape_ok(H_q, H_kv, D, page_size, num_pages, R, page_table_stride)) return INKLING_ERR_ARG;
   if (!(scale == scale)) return INKLING_ERR_ARG;
   if (B == 0) return INKLING_OK;
@@ -215,6 +221,7 @@ int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_ca
   c.seq_lens = seq_lens;
   c.rel = rel_logits;
   c.B = B;
+  c.QL = q_len;
   c.H_q = H_q;
   c.H_kv = H_kv;
   c.D = D;
@@ -223,19 +230,17 @@ int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_ca
   c.R = R;
   c.window = window;
   c.scale = scale;
-  c.keys_max = decode_keys_max(window, max_seq_len);
-  const int32_t S_req =
-      num_splits > 0 ? num_splits : inkling_rel_attn_choose_splits(B, H_kv, window, max_seq_len, di.sms);
-  decode_split_plan(c.keys_max, S_req, &c.S, &c.chunk);
+  decode_call_plan(B, q_len, H_q, H_kv, window, max_seq_len, num_splits, di.sms, &c.keys_max,
+                   &c.S, &c.chunk);
   c.out = out;
   c.lse_out = lse_out;
   c.o_part = nullptr;
   c.lse_part = nullptr;
   c.counter = nullptr;
   if (c.S > 1) {
-    const size_t need = decode_workspace_bytes(B, H_q, D, c.S);
+    const size_t need = decode_workspace_bytes(B * q_len, H_q, D, c.S);
     if (!workspace || workspace_bytes < need) return INKLING_ERR_WORKSPACE;
-    const size_t rows = (size_t)B * H_q * c.S;
+    const size_t rows = (size_t)B * q_len * H_q * c.S;
     char* ws = static_cast<char*>(workspace);
     c.counter = reinterpret_cast<int32_t*>(ws);
     c.o_part = reinterpret_cast<float*>(ws + 256);
@@ -244,6 +249,59 @@ int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_ca
   c.dev_err = device_error;
   c.stream = static_cast<cudaStream_t>(stream);
   return launch_decode(c);
+}
+}  // namespace ira
+
+extern "C" {
+
+size_t inkling_rel_attn_decode_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                                              int32_t window, int32_t max_seq_len,
+                                              int32_t num_splits, int32_t num_sms) {
+  return inkling_rel_attn_decode_multi_workspace_size(B, 1, H_q, H_kv, D, window, max_seq_len,
+                                                      num_splits, num_sms);
+}
+
+size_t inkling_rel_attn_decode_multi_workspace_size(int32_t B, int32_t q_len, int32_t H_q,
+                                                    int32_t H_kv, int32_t D, int32_t window,
+                                                    int32_t max_seq_len, int32_t num_splits,
+                                                    int32_t num_sms) {
+  if (B <= 0 || q_len < 1 || H_q <= 0 || H_kv <= 0) return 0;
+  int32_t keys, S, chunk;
+  decode_call_plan(B, q_len, H_q, H_kv, window, max_seq_len, num_splits, num_sms, &keys, &S,
+                   &chunk);
+  return decode_workspace_bytes(B * q_len, H_q, D, S);
+}
+
+size_t inkling_rel_attn_prefill_workspace_size(int32_t T, int32_t H_q, int32_t D) {
+  (void)T;
+  (void)H_q;
+  (void)D;
+  return 0;
+}
+
+int inkling_rel_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* page_table, int32_t page_table_stride,
+                            const int32_t* seq_lens, const float* rel_logits, int32_t B, int32_t H_q,
+                            int32_t H_kv, int32_t D, int32_t page_size, int32_t num_pages, int32_t R,
+                            int32_t window, float scale, int32_t max_seq_len, void* out,
+                            float* lse_out, void* workspace, size_t workspace_bytes,
+                            int32_t num_splits, int32_t* device_error, void* stream) {
+  return decode_call(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, rel_logits, B, 1,
+                     H_q, H_kv, D, page_size, num_pages, R, window, scale, max_seq_len, out,
+                     lse_out, workspace, workspace_bytes, num_splits, device_error, stream);
+}
+
+int inkling_rel_attn_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* page_table, int32_t page_table_stride,
+                                  const int32_t* seq_lens, const float* rel_logits, int32_t B,
+                                  int32_t q_len, int32_t H_q, int32_t H_kv, int32_t D,
+                                  int32_t page_size, int32_t num_pages, int32_t R, int32_t window,
+                                  float scale, int32_t max_seq_len, void* out, float* lse_out,
+                                  void* workspace, size_t workspace_bytes, int32_t num_splits,
+                                  int32_t* device_error, void* stream) {
+  return decode_call(q, k_cache, v_cache, page_table, page_table_stride, seq_lens, rel_logits, B,
+                     q_len, H_q, H_kv, D, page_size, num_pages, R, window, scale, max_seq_len, out,
+                     lse_out, workspace, workspace_bytes, num_splits, device_error, stream);
 }
 
 int inkling_rel_attn_prefill(const void* q, const int32_t* cu_seqlens_q, const void* k_cache,

@@ -77,35 +77,64 @@ struct DecodeParams {
   int32_t* dev_err;
   int32_t* counter;  // dynamic scheduling (zeroed before launch), or nullptr
   int B, pt_stride, H_q, H_kv, G, P, num_pages, R, window;
+  int QL, TG, NG;  // query tokens per sequence, tokens per item (group), groups per sequence
   int S, chunk, stages;
   int bias_prefetch;  // rel_logits rows are 16-byte aligned: L2 prefetch allowed
   float scale_log2;
 };
 
-// Visible key range [lo, pos] of the decode query of a sequence and its split
-// count; identical in the decode and merge kernels.
+// Visible key range [lo, pos] of token group `grp` of a sequence -- its
+// queries are tokens first .. first + tn - 1 of the sequence's last QL tokens,
+// at positions pos - tn + 1 .. pos; lo is the first one's window start -- and
+// the sequence's split count (the same for all its groups: the largest any
+// group needs).  Identical in the decode and merge kernels.  A sequence with
+// fewer than QL tokens has nothing visible (the host validates lengths; the
+// kernel reports it).
 struct SeqPlan {
-  int L, pos, lo, nvis, n_s;
+  int L, pos, lo, nvis, n_s, first, tn;
 };
+template <bool MULTI>
 __device__ __forceinline__ SeqPlan seq_plan(int L, int pt_stride, int P, int window, int chunk,
-                                            int S) {
+                                            int S, int QL, int TG, int NG, int grp) {
   SeqPlan s;
   const int cap = pt_stride * P;
   if (L > cap) L = cap;
   if (L < 0) L = 0;
   s.L = L;
-  s.pos = L - 1;
-  s.lo = (window > 0) ? max(0, s.pos - window + 1) : 0;
-  s.nvis = L > 0 ? s.pos - s.lo + 1 : 0;
-  int n = (s.nvis + chunk - 1) / chunk;
-  s.n_s = n > S ? S : n;
+  if constexpr (!MULTI) {  // one query token, at position L - 1
+    s.first = 0;
+    s.tn = 1;
+    s.pos = L - 1;
+    s.lo = (window > 0) ? max(0, s.pos - window + 1) : 0;
+    s.nvis = L > 0 ? s.pos - s.lo + 1 : 0;
+    const int n = (s.nvis + chunk - 1) / chunk;
+    s.n_s = n > S ? S : n;
+    return s;
+  }
+  s.first = grp * TG;
+  s.tn = min(TG, QL - s.first);
+  const bool ok = L >= QL;
+  s.pos = L - QL + s.first + s.tn - 1;
+  s.lo = (window > 0) ? max(0, s.pos - s.tn + 1 - window + 1) : 0;
+  s.nvis = ok ? s.pos - s.lo + 1 : 0;
+  int nmax = 0;
+  if (ok) {
+    for (int g = 0; g < NG; ++g) {  // every group's key count
+      const int tn = min(TG, QL - g * TG);
+      const int pos = L - QL + g * TG + tn - 1;
+      const int lo = (window > 0) ? max(0, pos - tn + 1 - window + 1) : 0;
+      nmax = max(nmax, (pos - lo + chunk) / chunk);
+    }
+  }
+  s.n_s = nmax > S ? S : nmax;
   return s;
 }
 
 // One work item as published by the producer: keys [a, e] of sequence b,
-// KV head hkv, split `split` of n_s; the decode query sits at pos.
+// KV head hkv, token group starting at packed token t0 with tn tokens (the
+// last at position pos), split `split` of n_s (a > e: nothing in this split).
 struct ItemRec {
-  int b, hkv, split, n_s, a, e, pos, nvis;
+  int b, hkv, split, n_s, a, e, pos, nvis, t0, tn;
 };
 
 // Shared-memory layout (byte offsets from the 1024-aligned base), computed
@@ -125,7 +154,10 @@ struct DecodeSmem {
   }
 };
 
-template <int D, int NT, int BH>
+// MULTI: several query tokens per sequence (the rows of an item are
+// (token, head) pairs, each with its own position, mask and bias row); the
+// single-token instantiations keep the plain per-key mask.
+template <int D, int NT, int BH, bool MULTI>
 __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int HALVES = D / 64;
@@ -142,13 +174,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   const int lane = tid & 31;
   const int G = p.G;
   const int S = p.S;
+  const int NR = p.TG * G;   // rows (token, head) of a full item
   const bool dense = S > 1;  // items enumerated through a per-sequence prefix sum
-  const DecodeSmem L(D, G, NT, p.stages, dense ? p.B + 1 : 0);
+  const DecodeSmem L(D, NR, NT, p.stages, dense ? p.B + 1 : 0);
   const int stages = L.stages;
   const int STAGE_BYTES = L.stage_bytes;
 
-  float* comb_o = reinterpret_cast<float*>(smem + L.comb_off);  // [4][G][D+4]
-  float* comb_m = comb_o + kConsumerWarps * G * (D + 4);          // [4][HP]
+  float* comb_o = reinterpret_cast<float*>(smem + L.comb_off);  // [4][NR][D+4]
+  float* comb_m = comb_o + kConsumerWarps * NR * (D + 4);         // [4][HP]
   float* comb_l = comb_m + kConsumerWarps * HP;                   // [4][HP]
   int* prefix = reinterpret_cast<int*>(smem + L.pre_off);         // [B+1] items before b
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
@@ -181,16 +214,17 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     }
     const uint64_t pol = policy_evict_first();
 
-    // dense item space: prefix[b] = items of sequences < b (H_kv * max(n_s, 1) each)
-    int total = p.B * p.H_kv;
+    // dense item space: prefix[b] = items of sequences < b (H_kv * NG * max(n_s, 1) each)
+    int total = p.B * p.H_kv * p.NG;
     if (dense) {
       int carry = 0;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
         int cnt = 0;
         if (b < p.B) {
-          const SeqPlan sp = seq_plan(__ldg(p.seq_lens + b), p.pt_stride, p.P, p.window, p.chunk, S);
-          cnt = p.H_kv * max(sp.n_s, 1);
+          const SeqPlan sp = seq_plan<MULTI>(__ldg(p.seq_lens + b), p.pt_stride, p.P, p.window,
+                                             p.chunk, S, p.QL, p.TG, p.NG, 0);
+          cnt = p.H_kv * p.NG * max(sp.n_s, 1);
         }
         int incl = cnt;
 #pragma unroll
@@ -206,8 +240,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       __syncwarp();
     }
 
-    // item id -> (b, hkv, split) and its key range
-    auto locate = [&](int id, int& b, int& hkv, int& split) {
+    // item id -> (b, hkv, token group, split) and its key range
+    auto locate = [&](int id, int& b, int& hkv, int& grp, int& split) {
       if (dense) {
         int lo = 0, hi = p.B - 1;  // last b with prefix[b] <= id
         while (lo < hi) {
@@ -217,12 +251,28 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         }
         b = lo;
         const int rest = id - prefix[b];
-        const int nsb = (prefix[b + 1] - prefix[b]) / p.H_kv;
-        hkv = rest / nsb;
-        split = rest - hkv * nsb;
+        if constexpr (MULTI) {
+          const int nsb = (prefix[b + 1] - prefix[b]) / (p.H_kv * p.NG);
+          hkv = rest / (p.NG * nsb);
+          const int rest2 = rest - hkv * p.NG * nsb;
+          grp = rest2 / nsb;
+          split = rest2 - grp * nsb;
+        } else {
+          const int nsb = (prefix[b + 1] - prefix[b]) / p.H_kv;
+          hkv = rest / nsb;
+          grp = 0;
+          split = rest - hkv * nsb;
+        }
+      } else if constexpr (MULTI) {
+        b = id / (p.H_kv * p.NG);
+        const int rest = id - b * p.H_kv * p.NG;
+        hkv = rest / p.NG;
+        grp = rest - hkv * p.NG;
+        split = 0;
       } else {
         b = id / p.H_kv;
         hkv = id - b * p.H_kv;
+        grp = 0;
         split = 0;
       }
     };
@@ -241,23 +291,30 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     auto resolve = [&](int id, int Lraw) -> ItemRec {
       ItemRec r;
       r.b = -1;
-      r.hkv = r.split = r.n_s = r.a = r.e = r.pos = r.nvis = 0;
+      r.hkv = r.split = r.n_s = r.a = r.e = r.pos = r.nvis = r.t0 = r.tn = 0;
       if (id >= total) return r;
-      locate(id, r.b, r.hkv, r.split);
-      const SeqPlan sp = seq_plan(Lraw, p.pt_stride, p.P, p.window, p.chunk, S);
-      if (Lraw > p.pt_stride * p.P && lane == 0 && r.hkv == 0 && r.split == 0)
-        report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
+      int grp;
+      locate(id, r.b, r.hkv, grp, r.split);
+      const SeqPlan sp =
+          seq_plan<MULTI>(Lraw, p.pt_stride, p.P, p.window, p.chunk, S, p.QL, p.TG, p.NG, grp);
+      if (lane == 0 && r.hkv == 0 && r.split == 0 && grp == 0) {
+        if (Lraw > p.pt_stride * p.P) report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
+        if (MULTI && Lraw < p.QL) report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);
+      }
       r.n_s = sp.n_s;
       r.pos = sp.pos;
       r.nvis = sp.nvis;
+      r.t0 = r.b * p.QL + sp.first;
+      r.tn = sp.tn;
       r.a = sp.lo + r.split * p.chunk;
-      r.e = (r.split >= sp.n_s - 1) ? sp.pos : r.a + p.chunk - 1;
+      if constexpr (MULTI) r.e = (r.split >= sp.n_s - 1) ? sp.pos : min(r.a + p.chunk - 1, sp.pos);
+      else r.e = (r.split >= sp.n_s - 1) ? sp.pos : r.a + p.chunk - 1;
       return r;
     };
     auto seq_len_of = [&](int id) -> int {  // issued early, consumed later
       if (id >= total) return 0;
-      int b, h, s;
-      locate(id, b, h, s);
+      int b, h, gr, s;
+      locate(id, b, h, gr, s);
       return __ldg(p.seq_lens + b);
     };
 
@@ -276,14 +333,32 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         *slot_rec(slot) = r;
         const uint32_t fb = smem_u32(&rfull[slot]);
         if (r.b >= 0 && r.nvis > 0) {
-          const uint32_t qbytes = G * D * 2;
-          mbar_arrive_expect_tx(fb, qbytes);
-          bulk_load(smem_u32(slot_q(slot)), p.q + ((size_t)r.b * p.H_q + r.hkv * G) * D, qbytes, fb);
+          // q rows (token i, head gh) in order i * G + gh: one copy per token
+          const uint32_t tbytes = G * D * 2;
+          if constexpr (MULTI) {
+            mbar_arrive_expect_tx(fb, r.tn * tbytes);
+            for (int i = 0; i < r.tn; ++i)
+              bulk_load(smem_u32(slot_q(slot)) + i * tbytes,
+                        p.q + ((size_t)(r.t0 + i) * p.H_q + r.hkv * G) * D, tbytes, fb);
+          } else {
+            mbar_arrive_expect_tx(fb, tbytes);
+            bulk_load(smem_u32(slot_q(slot)), p.q + ((size_t)r.b * p.H_q + r.hkv * G) * D, tbytes,
+                      fb);
+          }
         } else {
           mbar_arrive(fb);
         }
       }
-      if (r.b >= 0 && r.nvis > 0 && p.bias_prefetch && lane < G) {
+      if constexpr (MULTI) {
+        if (r.b >= 0 && r.nvis > 0 && r.a <= r.e && p.bias_prefetch && lane < r.tn * G) {
+          const int i = lane / G, gh = lane - (lane / G) * G;
+          const int pr = r.pos - (r.tn - 1) + i;  // this row's position
+          const int dlo = max(0, min(pr - r.e, p.R - 1)) & ~3;
+          const int dhi = min(max(0, min(pr - r.a, p.R - 1)) + 4, p.R) & ~3;
+          const float* row = p.rel + ((size_t)(r.t0 + i) * p.H_q + r.hkv * G + gh) * p.R;
+          if (dhi > dlo) bulk_prefetch_l2(row + dlo, (uint32_t)(dhi - dlo) * 4);
+        }
+      } else if (r.b >= 0 && r.nvis > 0 && p.bias_prefetch && lane < G) {
         const int dlo = min(r.pos - r.e, p.R - 1) & ~3;
         const int dhi = min(min(r.pos - r.a, p.R - 1) + 4, p.R) & ~3;
         const float* row = p.rel + ((size_t)r.b * p.H_q + r.hkv * G + lane) * p.R;
@@ -338,7 +413,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         nxt_done = true;
       };
       int local = 0;
-      if (cur.nvis > 0) {
+      if (cur.nvis > 0 && (!MULTI || cur.a <= cur.e)) {
         if constexpr (BH == 64) {
           PlanBig plan(cur.a, cur.e, p.P);
           while (!plan.done()) {
@@ -455,13 +530,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     }
     const ItemRec r = *slot_rec(slot);
     const bool final_out = r.n_s <= 1;
+    const int NRi = MULTI ? r.tn * G : G;  // live rows of this item
     uint32_t qf[KS][NT][2];
     if (r.b >= 0 && r.nvis > 0) {
       const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(slot_q(slot));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int head = nt * 8 + g;
-        const bool live = head < G;
+        const bool live = head < NRi;
         const __nv_bfloat16* qrow = qs + (live ? head : 0) * D;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -474,17 +550,54 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));  // slot free: q is in registers
     if (r.b < 0) break;
 
-    if (r.nvis == 0) {  // empty sequence: out = 0, lse = -inf
-      for (int i = tid; i < G * D; i += kConsumerThreads) {
-        const int h = i / D, d = i - h * D;
-        const size_t row = (size_t)r.b * p.H_q + r.hkv * G + h;
+    // output row of item row rr = (token i, head gh)
+    auto out_row = [&](int rr) -> size_t {
+      if constexpr (MULTI) {
+        const int i = rr / G;
+        return (size_t)(r.t0 + i) * p.H_q + r.hkv * G + (rr - i * G);
+      } else {
+        return (size_t)r.b * p.H_q + r.hkv * G + rr;
+      }
+    };
+    if (r.nvis == 0) {  // nothing visible: out = 0, lse = -inf
+      for (int i = tid; i < NRi * D; i += kConsumerThreads) {
+        const int rr = i / D, d = i - rr * D;
+        const size_t row = out_row(rr);
         p.out[row * D + d] = __float2bfloat16(0.f);
         if (d == 0 && p.lse_out) p.lse_out[row] = -INFINITY;
       }
       continue;
     }
+    if (MULTI && r.a > r.e) {  // a split past this group's keys: an empty partial
+      for (int i = tid; i < NRi * D; i += kConsumerThreads) {
+        const int rr = i / D, d = i - rr * D;
+        const size_t row = out_row(rr);
+        p.o_part[(row * S + r.split) * D + d] = 0.f;
+        if (d == 0) p.lse_part[row * S + r.split] = -INFINITY;
+      }
+      continue;
+    }
 
     const float* rel_g = p.rel + ((size_t)r.b * p.H_q + r.hkv * G) * R;
+    // MULTI: position and bias row of this thread's 2 * NT score rows
+    int row_pos[NT][2];
+    const float* row_rel[NT][2];
+    if constexpr (MULTI) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          int rr = nt * 8 + 2 * c4 + j;
+          rr = rr < NRi ? rr : NRi - 1;
+          const int i = rr / G;
+          row_pos[nt][j] = r.pos - (r.tn - 1) + i;
+          row_rel[nt][j] = p.rel + ((size_t)(r.t0 + i) * p.H_q + r.hkv * G + (rr - i * G)) * R;
+        }
+    }
+    // key `key` seen by the row at position pr (MULTI: causal + window per row)
+    auto row_sees = [&](int key, int pr) {
+      return key <= pr && (p.window <= 0 || pr - key < p.window);
+    };
     // bias of this thread's 4*NT scores of a tile (already in L2; loaded one
     // tile ahead of its use)
     auto load_bias = [&](const Tile& t, float (&bv)[NT][4]) {
@@ -494,11 +607,17 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int key = key0 + g + 8 * (i >> 1);
-          int h = nt * 8 + 2 * c4 + (i & 1);
-          h = h < G ? h : G - 1;
-          const bool v = key >= t.klo && key <= t.khi;
-          const int dcl = v ? min(r.pos - key, R - 1) : 0;
-          bv[nt][i] = __ldg(rel_g + (size_t)h * R + dcl);
+          if constexpr (MULTI) {
+            const int pr = row_pos[nt][i & 1];
+            const bool v = key >= t.klo && key <= t.khi && row_sees(key, pr);
+            bv[nt][i] = __ldg(row_rel[nt][i & 1] + (v ? min(pr - key, R - 1) : 0));
+          } else {
+            int h = nt * 8 + 2 * c4 + (i & 1);
+            h = h < G ? h : G - 1;
+            const bool v = key >= t.klo && key <= t.khi;
+            const int dcl = v ? min(r.pos - key, R - 1) : 0;
+            bv[nt][i] = __ldg(rel_g + (size_t)h * R + dcl);
+          }
         }
     };
 
@@ -551,7 +670,9 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         for (int i = 0; i < 4; ++i) {
           const int kr = i >> 1;
           const float s = fmaf(sacc[nt][i], sl2, bv[nt][i] * kLog2e);
-          sacc[nt][i] = vk[kr] ? s : -INFINITY;
+          bool ok_k = vk[kr];
+          if constexpr (MULTI) ok_k = ok_k && row_sees(key0 + g + 8 * kr, row_pos[nt][i & 1]);
+          sacc[nt][i] = ok_k ? s : -INFINITY;
         }
       }
 
@@ -676,9 +797,9 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int head = nt * 8 + 2 * c4 + (i & 1);
-          if (head < G) {
+          if (head < NRi) {
             const int dim = 16 * mt + g + 8 * (i >> 1);
-            comb_o[(warp * G + head) * OP + dim] = o_acc[mt][nt][i];
+            comb_o[(warp * NR + head) * OP + dim] = o_acc[mt][nt][i];
           }
         }
     if (g == 0) {
@@ -692,21 +813,33 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         }
     }
     named_bar_sync(1, kConsumerThreads);
-    for (int i = tid; i < G * D; i += kConsumerThreads) {
+    for (int i = tid; i < NRi * D; i += kConsumerThreads) {
       const int h = i / D, d = i - h * D;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * HP + h]);
       float Ls = 0.f, o = 0.f;
+      // MULTI, M = -inf: no key of this item is visible to the row (a split
+      // may lie wholly past a row's position): an empty result, o = 0 and
+      // lse = -inf, which the merge weighs at zero.  With one token every key
+      // of an item is visible to its rows.
+      if (!MULTI || M > -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float sc = ex2(comb_m[w * HP + h] - M);
-        Ls = fmaf(sc, comb_l[w * HP + h], Ls);
-        o = fmaf(sc, comb_o[(w * G + h) * OP + d], o);
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float sc = ex2(comb_m[w * HP + h] - M);
+          Ls = fmaf(sc, comb_l[w * HP + h], Ls);
+          o = fmaf(sc, comb_o[(w * NR + h) * OP + d], o);
+        }
       }
-      o = o / Ls;
-      const float lse = (M + log2f(Ls)) * kLn2;
-      const size_t row = (size_t)r.b * p.H_q + r.hkv * G + h;
+      float lse;
+      if constexpr (MULTI) {
+        o = Ls > 0.f ? o / Ls : 0.f;
+        lse = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+      } else {
+        o = o / Ls;
+        lse = (M + log2f(Ls)) * kLn2;
+      }
+      const size_t row = out_row(h);
       if (final_out) {
         p.out[row * D + d] = __float2bfloat16(o);
         if (d == 0 && p.lse_out) p.lse_out[row] = lse;
@@ -721,24 +854,27 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 
 // ---------------------------------------------------------------------------
 // Merge: out = sum_s exp(lse_s - LSE) o_s, LSE = log sum_s exp(lse_s).
-// One warp per (sequence, query head); sequences that used one split were
-// written directly by the decode kernel and are skipped.
+// One warp per (query token, query head); sequences that used one split were
+// written directly by the decode kernel and are skipped.  Empty splits carry
+// lse = -inf and weigh nothing.
 struct MergeParams {
   const int32_t* seq_lens;
   const float* o_part;
   const float* lse_part;
   __nv_bfloat16* out;
   float* lse_out;
-  int B, H_q, pt_stride, P, window, chunk, S;
+  int B, H_q, pt_stride, P, window, chunk, S, QL, TG, NG;
 };
 
-template <int D>
+template <int D, bool MULTI>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int idx = blockIdx.x * 4 + warp;
-  if (idx >= p.B * p.H_q) return;
-  const int b = idx / p.H_q;
-  const SeqPlan sp = seq_plan(p.seq_lens[b], p.pt_stride, p.P, p.window, p.chunk, p.S);
+  const int idx = blockIdx.x * 4 + warp;  // (packed token, head)
+  if (idx >= p.B * p.QL * p.H_q) return;
+  const int t = idx / p.H_q;
+  const int b = t / p.QL;
+  const SeqPlan sp = seq_plan<MULTI>(p.seq_lens[b], p.pt_stride, p.P, p.window, p.chunk, p.S,
+                                     p.QL, p.TG, p.NG, (t - b * p.QL) / p.TG);
   const int n = sp.n_s;
   if (n <= 1) return;
   const float* lse = p.lse_part + (size_t)idx * p.S;
@@ -750,13 +886,13 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
   for (int s = lane; s < n; s += 32) z += ex2((lse[s] - M) * kLog2e);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-  const float LSE = M + logf(z);
+  const float LSE = M > -INFINITY ? M + logf(z) : -INFINITY;
   constexpr int PER = D / 32;
   float acc[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) acc[j] = 0.f;
   const float* o = p.o_part + (size_t)idx * p.S * D + lane * PER;
-  for (int s = 0; s < n; ++s) {
+  for (int s = 0; s < n && LSE > -INFINITY; ++s) {
     const float w = ex2((lse[s] - LSE) * kLog2e);
     if constexpr (PER == 4) {
       const float4 v = *reinterpret_cast<const float4*>(o + (size_t)s * D);
@@ -786,9 +922,9 @@ static int sm_count() {
   return n;
 }
 
-template <int D, int NT, int BH>
+template <int D, int NT, int BH, bool MULTI>
 static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int smem_bytes, int grid) {
-  auto kern = decode_kernel<D, NT, BH>;
+  auto kern = decode_kernel<D, NT, BH, MULTI>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -817,7 +953,13 @@ int launch_decode(const DecodeCall& c) {
       return INKLING_ERR_CUDA;
   }
   const int G = c.H_q / c.H_kv;
-  const int NT = (G <= 8) ? 1 : 2;
+  // several query tokens per sequence: items take groups of TG tokens, TG * G
+  // rows at most 16 (two 8-row MMA tiles); each group reads its K/V once
+  const int QL = std::max(1, c.QL);
+  const int TG = decode_token_group(QL, G);
+  const int NG = (QL + TG - 1) / TG;
+  const int NR = TG * G;
+  const int NT = (NR <= 8) ? 1 : 2;
   prm.q = static_cast<const __nv_bfloat16*>(c.q);
   prm.page_table = c.page_table;
   prm.seq_lens = c.seq_lens;
@@ -837,6 +979,9 @@ int launch_decode(const DecodeCall& c) {
   prm.num_pages = c.num_pages;
   prm.R = c.R;
   prm.window = c.window;
+  prm.QL = QL;
+  prm.TG = TG;
+  prm.NG = NG;
   prm.S = c.S;
   prm.chunk = c.chunk;
   prm.scale_log2 = c.scale * kLog2e;
@@ -845,15 +990,15 @@ int launch_decode(const DecodeCall& c) {
   // kCtasPerSm CTAs per SM: keep each CTA under the budget; 2..max stages
   const int budget = INKLING_DECODE_SMEM_BUDGET_KB * 1024;
   int stages = INKLING_DECODE_MAX_STAGES;
-  while (stages > 2 && DecodeSmem(c.D, G, NT, stages, n_prefix).total > budget) --stages;
+  while (stages > 2 && DecodeSmem(c.D, NR, NT, stages, n_prefix).total > budget) --stages;
   prm.stages = stages;
-  const int smem = 1024 + DecodeSmem(c.D, G, NT, stages, n_prefix).total;
+  const int smem = 1024 + DecodeSmem(c.D, NR, NT, stages, n_prefix).total;
   if (smem > 227 * 1024) return INKLING_ERR_ARG;  // batch too large for the item prefix table
 
   // Static schedule (one split per sequence): give every CTA the same number
   // of items (a grid of ceil(items / waves) CTAs), so the last wave is not a
   // partial one.  Dynamic schedule (splits): fill every slot.
-  const int total_items = c.B * c.H_kv * c.S;
+  const int total_items = c.B * c.H_kv * NG * c.S;
   const int slots = kCtasPerSm * sm_count();
   int grid = std::min(total_items, slots);
   if (!c.counter && INKLING_DECODE_BALANCED) {
@@ -865,20 +1010,38 @@ int launch_decode(const DecodeCall& c) {
     return INKLING_ERR_CUDA;
 
   int rc;
-  if (c.D == 128) {
-    if (BH == 64)
-      rc = NT == 1 ? launch_decode_t<128, 1, 64>(c, prm, smem, grid)
-                   : launch_decode_t<128, 2, 64>(c, prm, smem, grid);
-    else
-      rc = NT == 1 ? launch_decode_t<128, 1, 16>(c, prm, smem, grid)
-                   : launch_decode_t<128, 2, 16>(c, prm, smem, grid);
+  if (QL == 1) {
+    if (c.D == 128) {
+      if (BH == 64)
+        rc = NT == 1 ? launch_decode_t<128, 1, 64, false>(c, prm, smem, grid)
+                     : launch_decode_t<128, 2, 64, false>(c, prm, smem, grid);
+      else
+        rc = NT == 1 ? launch_decode_t<128, 1, 16, false>(c, prm, smem, grid)
+                     : launch_decode_t<128, 2, 16, false>(c, prm, smem, grid);
+    } else {
+      if (BH == 64)
+        rc = NT == 1 ? launch_decode_t<64, 1, 64, false>(c, prm, smem, grid)
+                     : launch_decode_t<64, 2, 64, false>(c, prm, smem, grid);
+      else
+        rc = NT == 1 ? launch_decode_t<64, 1, 16, false>(c, prm, smem, grid)
+                     : launch_decode_t<64, 2, 16, false>(c, prm, smem, grid);
+    }
   } else {
-    if (BH == 64)
-      rc = NT == 1 ? launch_decode_t<64, 1, 64>(c, prm, smem, grid)
-                   : launch_decode_t<64, 2, 64>(c, prm, smem, grid);
-    else
-      rc = NT == 1 ? launch_decode_t<64, 1, 16>(c, prm, smem, grid)
-                   : launch_decode_t<64, 2, 16>(c, prm, smem, grid);
+    if (c.D == 128) {
+      if (BH == 64)
+        rc = NT == 1 ? launch_decode_t<128, 1, 64, true>(c, prm, smem, grid)
+                     : launch_decode_t<128, 2, 64, true>(c, prm, smem, grid);
+      else
+        rc = NT == 1 ? launch_decode_t<128, 1, 16, true>(c, prm, smem, grid)
+                     : launch_decode_t<128, 2, 16, true>(c, prm, smem, grid);
+    } else {
+      if (BH == 64)
+        rc = NT == 1 ? launch_decode_t<64, 1, 64, true>(c, prm, smem, grid)
+                     : launch_decode_t<64, 2, 64, true>(c, prm, smem, grid);
+      else
+        rc = NT == 1 ? launch_decode_t<64, 1, 16, true>(c, prm, smem, grid)
+                     : launch_decode_t<64, 2, 16, true>(c, prm, smem, grid);
+    }
   }
   if (rc != INKLING_OK || c.S <= 1) return rc;
 
@@ -895,11 +1058,17 @@ int launch_decode(const DecodeCall& c) {
   mp.window = c.window;
   mp.chunk = c.chunk;
   mp.S = c.S;
-  const int blocks = (c.B * c.H_q + 3) / 4;
-  if (c.D == 128)
-    merge_kernel<128><<<blocks, 128, 0, c.stream>>>(mp);
-  else
-    merge_kernel<64><<<blocks, 128, 0, c.stream>>>(mp);
+  mp.QL = QL;
+  mp.TG = TG;
+  mp.NG = NG;
+  const int blocks = (int)(((int64_t)c.B * QL * c.H_q + 3) / 4);
+  if (QL == 1) {
+    if (c.D == 128) merge_kernel<128, false><<<blocks, 128, 0, c.stream>>>(mp);
+    else merge_kernel<64, false><<<blocks, 128, 0, c.stream>>>(mp);
+  } else {
+    if (c.D == 128) merge_kernel<128, true><<<blocks, 128, 0, c.stream>>>(mp);
+    else merge_kernel<64, true><<<blocks, 128, 0, c.stream>>>(mp);
+  }
   if (cudaGetLastError() != cudaSuccess) return INKLING_ERR_CUDA;
   return INKLING_OK;
 }

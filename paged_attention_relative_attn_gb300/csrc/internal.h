@@ -20,14 +20,15 @@ struct DecodeCall {
   const int32_t* seq_lens;
   const float* rel;
   int32_t B, H_q, H_kv, D, P, num_pages, R, window;
+  int32_t QL;        // query tokens per sequence (1: plain decode)
   float scale;
-  int32_t keys_max;  // host bound on visible keys per query
+  int32_t keys_max;  // host bound on visible keys per item
   int32_t S;         // split count (grid.x)
   int32_t chunk;     // keys per split (multiple of 64)
   void* out;
   float* lse_out;
-  float* o_part;     // [B, H_q, S, D] when S > 1
-  float* lse_part;   // [B, H_q, S]   when S > 1
+  float* o_part;     // [B * QL, H_q, S, D] when S > 1
+  float* lse_part;   // [B * QL, H_q, S]   when S > 1
   int32_t* counter;  // work-item counter (S > 1), zeroed by the launcher
   int32_t* dev_err;
   cudaStream_t stream;
@@ -73,6 +74,24 @@ int launch_kv_append(const KvAppendCall& c);   // returns INKLING_* code
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,
                   const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                   CUtensorMapSwizzle swizzle);
+
+// Multi-token decode: query tokens per item (token group) for q_len tokens per
+// sequence and G query heads per KV head -- the rows (token, head) of an item
+// fill at most 16 (two 8-row MMA tiles).  Shared by the ABI helpers and the
+// launcher so that the split plan and the kernel agree.
+// (one 8-row MMA tile when it still holds two tokens of the group: the math
+// per key halves while each K/V tile is read once per two tokens; else two
+// tiles.  INKLING_MTP_MAX_ROWS > 0 forces the bound.)
+#ifndef INKLING_MTP_MAX_ROWS
+#define INKLING_MTP_MAX_ROWS 0
+#endif
+inline int32_t decode_token_group(int32_t q_len, int32_t G) {
+  if (q_len <= 1) return 1;
+  const int32_t rows = INKLING_MTP_MAX_ROWS > 0 ? INKLING_MTP_MAX_ROWS : (2 * G <= 8 ? 8 : 16);
+  int32_t tg = G > 0 ? rows / G : 1;
+  if (tg < 1) tg = 1;
+  return tg < q_len ? tg : q_len;
+}
 
 // Split plan shared by the ABI helpers and the launcher.
 int32_t decode_keys_max(int32_t window, int32_t max_seq_len);

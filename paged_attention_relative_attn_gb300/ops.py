@@ -92,6 +92,54 @@ def decode(q, k_cache, v_cache, page_table, seq_lens, rel_logits, *, window, sca
     return out, lse
 
 
+def decode_multi_workspace_bytes(B, q_len, H_q, H_kv, D, window, max_seq_len, num_splits=0,
+                                 num_sms=0):
+    return _lib.inkling_rel_attn_decode_multi_workspace_size(B, q_len, H_q, H_kv, D, window,
+                                                             max_seq_len, num_splits, num_sms)
+
+
+def decode_multi(q, k_cache, v_cache, page_table, seq_lens, rel_logits, *, q_len, window, scale,
+                 max_seq_len, out=None, lse=None, workspace=None, num_splits=0,
+                 device_error=None, stream=None):
+    """Decode of ``q_len`` new tokens per sequence (the last q_len of each).
+    See inkling_rel_attn_decode_multi.
+
+    q [B * q_len, H_q, D] bf16 (row b * q_len + i); rel_logits [B * q_len, H_q, R]
+    fp32; other tensors as ``decode``.  Returns (out [B * q_len, H_q, D] bf16,
+    lse [B * q_len, H_q] fp32).
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(rel_logits, "rel_logits", torch.float32, 3)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    T, H_q, D = q.shape
+    B = seq_lens.shape[0]
+    num_pages, P, H_kv, Dk = k_cache.shape
+    R = rel_logits.shape[2]
+    if (Dk != D or T != B * q_len or rel_logits.shape[:2] != (T, H_q)
+            or page_table.shape[0] != B):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((T, H_q), dtype=torch.float32, device=q.device)
+    ws_need = decode_multi_workspace_bytes(B, q_len, H_q, H_kv, D, window, max_seq_len, num_splits)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.inkling_rel_attn_decode_multi(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
+        _ptr(seq_lens), _ptr(rel_logits), B, q_len, H_q, H_kv, D, P, num_pages, R, window,
+        float(scale), max_seq_len, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+        num_splits, _ptr(device_error), _stream(q.device, stream))
+    _check(rc, "inkling_rel_attn_decode_multi")
+    return out, lse
+
+
 def prefill(q, cu_seqlens_q, k_cache, v_cache, page_table, seq_lens, rel_logits, *, window,
             scale, max_seq_len, max_q_len, out=None, lse=None, device_error=None, stream=None):
     """Chunked / paged prefill.  See inkling_rel_attn_prefill.

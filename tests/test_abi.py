@@ -132,3 +132,27 @@ def test_kv_append_argument_validation(lib):
     assert rc(k_new=None) == -1
     assert rc(k_cache=24) == -2         # 16-byte alignment
     assert rc(seq_lens=6) == -2
+
+
+def test_decode_multi_validation_and_workspace(lib):
+    a = dict(q=16, k_cache=16, v_cache=16, page_table=4, page_table_stride=4, seq_lens=4,
+             rel_logits=4, B=2, q_len=4, H_q=4, H_kv=2, D=64, page_size=16, num_pages=16, R=32,
+             window=32, scale=0.125, max_seq_len=100, out=16, lse_out=None, workspace=None,
+             workspace_bytes=0, num_splits=0, device_error=None, stream=None)
+    rc = lambda **o: lib.inkling_rel_attn_decode_multi(**{**a, **o})  # noqa: E731
+    assert rc(q_len=0) == -1
+    assert rc(q_len=65) == -1
+    assert rc(max_seq_len=3) == -1          # fewer keys than new tokens
+    assert rc(D=96) == -1
+    assert rc(B=0) == 0
+    assert rc(q=24) == -2
+    # q_len = 1 is plain decode: same workspace
+    for args in ((32, 48, 8, 128, 0, 32768, 0, 152), (64, 48, 16, 128, 512, 8192, 0, 152),
+                 (1, 4, 2, 64, 0, 100, 50, 152)):
+        B, H_q, H_kv, D, W_, L, S, sms = args
+        assert (lib.inkling_rel_attn_decode_multi_workspace_size(B, 1, H_q, H_kv, D, W_, L, S, sms)
+                == lib.inkling_rel_attn_decode_workspace_size(B, H_q, H_kv, D, W_, L, S, sms))
+    # several tokens: partials for every (token, head, split)
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    ws = lib.inkling_rel_attn_decode_multi_workspace_size(2, 4, 12, 2, 128, 0, 40000, 8, 152)
+    assert ws == 256 + r256(2 * 4 * 12 * 8 * 128 * 4) + r256(2 * 4 * 12 * 8 * 4)
