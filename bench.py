@@ -204,6 +204,16 @@ def time_steps(args, device, step, K, warmup, per_graph):
     return ms, clk.summary()
 
 
+def decode_workload_config(name, batch=None):
+    """The static description of a decode workload (the same in both arms)."""
+    c = W.DECODE_CONFIGS[name]
+    B = c["B"] if batch is None else batch
+    lens = c.get("len_range")
+    return {"workload": name, "batch": B, "heads": f"{c['H_q']}/{c['H_kv']}", "head_dim": c["D"],
+            "page_size": c["P"], "window": c["window"], "R": c["R"],
+            "lengths": f"uniform [{lens[0]}, {lens[1]}]" if lens else "fixed"}
+
+
 def bench_decode(args, device, name, K, warmup):
     import paged_attention_relative_attn_gb300 as ira
     sets = []
@@ -235,10 +245,9 @@ def bench_decode(args, device, name, K, warmup):
     all_total = sum(per_set[i % n_sets][1] for i in range(K))
     launches = K * (1 + (1 if S > 1 else 0))
     x0 = sets[0]
-    config = {"workload": name, "batch": B, "heads": f"{H_q}/{H_kv}", "head_dim": D,
-              "page_size": x0.page_size, "window": x0.window, "R": x0.R, "num_splits": S,
-              "l2": f"rotating {n_sets} input sets, {sum(p[0] for p in per_set) / 1e6:.0f} MB of "
-                    f"visible K/V per rotation (L2 129 MB)"}
+    config = dict(decode_workload_config(name, args.batch), num_splits=S,
+                  l2=f"rotating {n_sets} input sets, {sum(p[0] for p in per_set) / 1e6:.0f} MB of "
+                     f"visible K/V per rotation (L2 129 MB)")
     return dict(ms=ms, K=K, clocks=clocks, launches=launches, config=config, sets=sets, ws=ws,
                 units_total=kv_total, bytes_total=all_total, kernel="decode_kernel",
                 kernel_launches=K, unit="GB/s")
@@ -644,7 +653,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload},
+            "data": "synthetic",
+            "config": decode_workload_config(args.workload, getattr(args, "batch", None)),
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
                              "sample": f"per step: (sequence, KV head) units of the first "
                                        f"{n_seq} sequences of {args.workload}, ~{per_step:.3f} s "

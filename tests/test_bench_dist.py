@@ -39,7 +39,7 @@ def _worker(rank, world, port, q):
     u = bench.sum_over_ranks(args, 100.0 * (rank + 1))  # units add up
     # the reference arm: rank 0 prints one line, the others print nothing
     rargs = types.SimpleNamespace(world=world, rank=rank, local=rank, workload="local_decode",
-                                  steps=1, warmup=0, ref_budget=0.01, gpus=world)
+                                  steps=1, warmup=0, ref_budget=0.01, gpus=world, batch=None)
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         bench.run_reference(rargs)
