@@ -1,8 +1,9 @@
 """Benchmark of the relative-bias paged attention hot path on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload local_decode|global_decode|chunked_prefill|decode_66_layers]
-                    [--no-cpu-baseline] [--extra]
+                    [--workload local_decode|global_decode|chunked_prefill|global_prefill|
+                                kv_append|mtp_decode|decode_66_layers]
+                    [--no-cpu-baseline] [--no-e2e] [--no-extra] [--batch B] [--sets S]
 
 Prints ONE JSON line (rank 0).  The default workload is the local-layer decode
 batch (B=64, 48/16 heads, D=128, page 64, lengths uniform in [1024, 8192],
@@ -12,6 +13,9 @@ sets whose visible K/V together exceed the 129 MB L2.  The timed region is a
 CUDA-graph replay of exactly K steps bracketed by events (and, for N > 1, a
 barrier with the max over ranks); ranks are independent replicas (the path
 has no exchange step), so scaling is weak.
+
+With the default workload the line also carries the other workloads (each
+with its own roofline) under ``extra_workloads`` unless ``--no-extra``.
 
 ``--impl reference`` times the CPU fp64 oracle instead (on this host's cores,
 rank 0 only, each step a bounded sample of the same workload).
