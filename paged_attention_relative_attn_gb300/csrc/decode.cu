@@ -163,6 +163,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   constexpr int HALVES = D / 64;
   constexpr int TILE_BYTES = HALVES * kHalfBytes;
   constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
+  // With one n-tile, QK^T accumulates over two chains (even / odd k-steps):
+  // the chain of dependent MMAs halves; two n-tiles already give two chains.
+  constexpr bool kTwoChains = NT == 1;
+  // O is rescaled only when some row's running max moved (warp vote); with
+  // one n-tile of multi-token rows the vote costs more than it saves.
+  constexpr bool kLazyRescale = !(MULTI && NT == 1);
   constexpr int HP = 8 * NT;  // padded heads per group
 
   extern __shared__ uint8_t smem_raw[];
@@ -642,10 +648,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
 
       // ---- S^T = K Q^T  (16 keys x 8*NT heads)
       float sacc[NT][4];
+      float sacc2[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
+        for (int i = 0; i < 4; ++i) {
+          sacc[nt][i] = 0.f;
+          sacc2[nt][i] = 0.f;
+        }
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int chunk = 2 * ks + k_chi;
@@ -654,8 +664,18 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         uint32_t a0, a1, a2, a3;
         ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (kTwoChains && (ks & 1))
+            mma_16816(sacc2[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+          else
+            mma_16816(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+        }
+      }
+      if constexpr (kTwoChains) {
+#pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-          mma_16816(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sacc[nt][i] += sacc2[nt][i];
       }
 
       // ---- scale + bias + mask (log2 domain)
@@ -701,6 +721,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         l_run[nt][1] = fmaf(l_run[nt][1], al1, p1 + p3);
         m_run[nt][0] = mn0;
         m_run[nt][1] = mn1;
+        if (!kLazyRescale || !__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f))
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           o_acc[mt][nt][0] *= al0;
