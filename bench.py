@@ -471,68 +471,107 @@ def bench_stack(args, device, K, warmup):
                 kernel_launches=K * len(layers), unit="GB/s")
 
 
-def bench_decode_e2e(args, device, sets, ws):
+def _packed_views(buf, specs):
+    """Views (dtype, shape) into one flat uint8 buffer at 256-byte aligned
+    offsets; returns (views, bytes used)."""
+    views, off = [], 0
+    for dtype, shape in specs:
+        n = torch.Size(shape).numel() * torch.empty((), dtype=dtype).element_size()
+        views.append(buf[off:off + n].view(dtype).view(shape))
+        off += (n + 255) // 256 * 256
+    return views, off
+
+
+def _packed_bytes(specs):
+    off = 0
+    for dtype, shape in specs:
+        n = torch.Size(shape).numel() * torch.empty((), dtype=dtype).element_size()
+        off += (n + 255) // 256 * 256
+    return off
+
+
+def bench_decode_e2e(args, device, sets, ws, nbuf=2):
     """Same metric through the public API with host buffers, the way a serving
     loop drives it: every step copies its per-step inputs (q, rel_logits,
     page_table, seq_lens) from pinned host memory, runs decode and reads out +
-    lse back to pinned host memory.  Inputs are double-buffered on the device
-    and step i+1's host-to-device copies run on a side stream while step i's
-    kernel runs; the calls of a rotation of steps are captured once in a CUDA
-    graph and replayed, so every timed step still performs its own copies.
-    The paged K/V cache is the model's resident state and stays in HBM."""
+    lse back to pinned host memory.  A step's inputs sit packed in one pinned
+    staging buffer and move in one host-to-device copy (each copy has a fixed
+    cost of several microseconds); out and lse are written into one device
+    buffer and move back in one copy.  Inputs and outputs are double-buffered
+    on the device: step i+1's upload runs on one side stream and step i-1's
+    download on another while step i's kernel runs.  The calls of a rotation
+    of steps are captured once in a CUDA graph and replayed, so every timed
+    step still performs its own copies.  The paged K/V cache is the model's
+    resident state and stays in HBM."""
     import paged_attention_relative_attn_gb300 as ira
     n = len(sets)
-    NB = 2  # device input / output buffers
-    host = []
+    NB = nbuf  # device input / output buffers
+    s0 = sets[0]
+    in_specs = [(s0.q.dtype, s0.q.shape), (s0.rel_logits.dtype, s0.rel_logits.shape),
+                (s0.page_table.dtype, s0.page_table.shape), (s0.seq_lens.dtype, s0.seq_lens.shape)]
+    out_specs = [(s0.q.dtype, s0.q.shape), (torch.float32, s0.q.shape[:2])]
+    in_bytes = _packed_bytes(in_specs)
+    out_bytes = _packed_bytes(out_specs)
+    host_in = []
     for s in sets:
-        host.append(dict(q=s.q.cpu().pin_memory(), rel=s.rel_logits.cpu().pin_memory(),
-                         pt=s.page_table.cpu().pin_memory(), sl=s.seq_lens.cpu().pin_memory()))
-    dq = [torch.empty_like(sets[0].q) for _ in range(NB)]
-    drel = [torch.empty_like(sets[0].rel_logits) for _ in range(NB)]
-    dpt = [torch.empty_like(sets[0].page_table) for _ in range(NB)]
-    dsl = [torch.empty_like(sets[0].seq_lens) for _ in range(NB)]
-    out = [torch.empty_like(sets[0].q) for _ in range(NB)]
-    lse = [torch.empty(sets[0].q.shape[:2], dtype=torch.float32, device=device) for _ in range(NB)]
-    h_out = [torch.empty(out[0].shape, dtype=out[0].dtype).pin_memory() for _ in range(NB)]
-    h_lse = [torch.empty(lse[0].shape, dtype=lse[0].dtype).pin_memory() for _ in range(NB)]
-    h2d = (host[0]["q"].numel() * 2 + host[0]["rel"].numel() * 4 + host[0]["pt"].numel() * 4 +
-           host[0]["sl"].numel() * 4)
-    d2h = h_out[0].numel() * 2 + h_lse[0].numel() * 4
+        hb = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        views, _ = _packed_views(hb, in_specs)
+        for v, t in zip(views, (s.q, s.rel_logits, s.page_table, s.seq_lens)):
+            v.copy_(t.cpu())
+        host_in.append(hb)
+    dev_in = [torch.empty(in_bytes, dtype=torch.uint8, device=device) for _ in range(NB)]
+    dev_in_v = [_packed_views(b, in_specs)[0] for b in dev_in]
+    dev_out = [torch.empty(out_bytes, dtype=torch.uint8, device=device) for _ in range(NB)]
+    dev_out_v = [_packed_views(b, out_specs)[0] for b in dev_out]
+    host_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(NB)]
     main = torch.cuda.Stream(device)
-    side = torch.cuda.Stream(device)  # host-to-device copies
+    up = torch.cuda.Stream(device)    # host-to-device copies
+    down = torch.cuda.Stream(device)  # device-to-host copies
     per = n * max(1, 32 // n)  # steps per graph replay (a whole number of rotations)
 
     def enqueue(steps):
-        side.wait_stream(main)
-        done = []
+        up.wait_stream(main)
+        down.wait_stream(main)
+        kdone, ddone = [], []
         for i in range(steps):
             b = i % NB
-            h = host[i % n]
             s = sets[i % n]
-            with torch.cuda.stream(side):
+            with torch.cuda.stream(up):
                 if i >= NB:
-                    side.wait_event(done[i - NB])  # buffer b is free again
-                dq[b].copy_(h["q"], non_blocking=True)
-                drel[b].copy_(h["rel"], non_blocking=True)
-                dpt[b].copy_(h["pt"], non_blocking=True)
-                dsl[b].copy_(h["sl"], non_blocking=True)
+                    up.wait_event(kdone[i - NB])  # step i-NB's kernel has read dev_in[b]
+                dev_in[b].copy_(host_in[i % n], non_blocking=True)
                 ready = torch.cuda.Event()
-                ready.record(side)
+                ready.record(up)
+            q, rel, pt, sl = dev_in_v[b]
+            out, lse = dev_out_v[b]
             with torch.cuda.stream(main):
                 main.wait_event(ready)
-                ira.decode(dq[b], s.k_cache, s.v_cache, dpt[b], dsl[b], drel[b], window=s.window,
-                           scale=s.scale, max_seq_len=s.max_seq_len, out=out[b], lse=lse[b],
+                if i >= NB:
+                    main.wait_event(ddone[i - NB])  # step i-NB's result has left dev_out[b]
+                ira.decode(q, s.k_cache, s.v_cache, pt, sl, rel, window=s.window,
+                           scale=s.scale, max_seq_len=s.max_seq_len, out=out, lse=lse,
                            workspace=ws, stream=main)
-                h_out[b].copy_(out[b], non_blocking=True)
-                h_lse[b].copy_(lse[b], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(main)
-                done.append(ev)
-        main.wait_stream(side)
+                kdone.append(ev)
+            with torch.cuda.stream(down):
+                down.wait_event(ev)
+                host_out[b].copy_(dev_out[b], non_blocking=True)
+                ev2 = torch.cuda.Event()
+                ev2.record(down)
+                ddone.append(ev2)
+        main.wait_stream(up)
+        main.wait_stream(down)
 
     main.wait_stream(torch.cuda.current_stream())
     enqueue(per)  # eager warm-up
     torch.cuda.synchronize()
+    # the packed round trip returns the same result as the direct call
+    ref_out, ref_lse = ira.decode_inputs(sets[(per - 1) % n])
+    torch.cuda.synchronize()
+    got_out, got_lse = _packed_views(host_out[(per - 1) % NB], out_specs)[0]
+    if not (torch.equal(got_out, ref_out.cpu()) and torch.equal(got_lse, ref_lse.cpu())):
+        raise RuntimeError("e2e: the packed round trip differs from the direct decode call")
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(main):
         with torch.cuda.graph(g, stream=main):
@@ -554,11 +593,12 @@ def bench_decode_e2e(args, device, sets, ws):
     wall = time.perf_counter() - t0
     ms = max(ev0.elapsed_time(ev1), wall * 1e3)
     kv = sum(decode_bytes(sets[i % n])[0] for i in range(K))
-    return dict(value=kv / (ms * 1e-3) / 1e9, unit="GB/s", h2d_bytes_per_step=h2d,
-                d2h_bytes_per_step=d2h, steps=K,
-                how="public API calls captured in a CUDA graph; per step: H2D of q, rel_logits, "
-                    "page_table, seq_lens from pinned host memory (double-buffered, overlapping the "
-                    "previous step's kernel), decode, D2H of out and lse to pinned host memory")
+    return dict(value=kv / (ms * 1e-3) / 1e9, unit="GB/s", h2d_bytes_per_step=in_bytes,
+                d2h_bytes_per_step=out_bytes, steps=K,
+                how="public API calls captured in a CUDA graph; per step: one H2D copy of the packed "
+                    "q, rel_logits, page_table, seq_lens from pinned host memory (double-buffered, "
+                    "overlapping the previous step's kernel), decode, one D2H copy of the packed "
+                    "out and lse to pinned host memory on a third stream")
 
 
 # ---------------------------------------------------------------------------
