@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "plan.cuh"
@@ -604,10 +605,30 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     auto row_sees = [&](int key, int pr) {
       return key <= pr && (p.window <= 0 || pr - key < p.window);
     };
+    // MULTI: every row of the group sees all 16 keys of this warp's slice
+    // (inside the tile's range, at or before the group's first position and
+    // inside the window of its last): no per-score mask, and every bias index
+    // pos - key is already >= 0.  Warp-uniform.
+    auto all_see = [&](const Tile& t, int key0) {
+      return key0 >= t.klo && key0 + 15 <= t.khi && key0 + 15 <= r.pos - (r.tn - 1) &&
+             (p.window <= 0 || r.pos - key0 < p.window);
+    };
     // bias of this thread's 4*NT scores of a tile (already in L2; loaded one
     // tile ahead of its use)
     auto load_bias = [&](const Tile& t, float (&bv)[NT][4]) {
       const int key0 = t.jbase + r0;
+      if constexpr (MULTI) {
+        if (all_see(t, key0)) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int key = key0 + g + 8 * (i >> 1);
+              bv[nt][i] = __ldg(row_rel[nt][i & 1] + min(row_pos[nt][i & 1] - key, R - 1));
+            }
+          return;
+        }
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -679,20 +700,27 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       }
 
       // ---- scale + bias + mask (log2 domain)
-      bool vk[2] = {true, true};  // validity of keys g, g+8
-      if (part) {
-        vk[0] = (key0 + g >= t.klo) && (key0 + g <= t.khi);
-        vk[1] = (key0 + g + 8 >= t.klo) && (key0 + g + 8 <= t.khi);
-      }
+      if (MULTI && all_see(t, key0)) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int kr = i >> 1;
-          const float s = fmaf(sacc[nt][i], sl2, bv[nt][i] * kLog2e);
-          bool ok_k = vk[kr];
-          if constexpr (MULTI) ok_k = ok_k && row_sees(key0 + g + 8 * kr, row_pos[nt][i & 1]);
-          sacc[nt][i] = ok_k ? s : -INFINITY;
+          for (int i = 0; i < 4; ++i) sacc[nt][i] = fmaf(sacc[nt][i], sl2, bv[nt][i] * kLog2e);
+      } else {
+        bool vk[2] = {true, true};  // validity of keys g, g+8
+        if (part) {
+          vk[0] = (key0 + g >= t.klo) && (key0 + g <= t.khi);
+          vk[1] = (key0 + g + 8 >= t.klo) && (key0 + g + 8 <= t.khi);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kr = i >> 1;
+            const float s = fmaf(sacc[nt][i], sl2, bv[nt][i] * kLog2e);
+            bool ok_k = vk[kr];
+            if constexpr (MULTI) ok_k = ok_k && row_sees(key0 + g + 8 * kr, row_pos[nt][i & 1]);
+            sacc[nt][i] = ok_k ? s : -INFINITY;
+          }
         }
       }
 
@@ -734,28 +762,34 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       }
 
       // ---- O^T += V^T P^T
-      uint32_t zm01 = 0xffffffffu, zm89 = 0xffffffffu;
+      auto pv = [&](uint32_t zm01, uint32_t zm89, auto masked) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int chunk = 2 * mt + v_chi;
+          const uint32_t addr =
+              vb + (chunk >> 3) * kHalfBytes + v_row * 128 + (((chunk & 7) ^ sw) << 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(addr, a0, a1, a2, a3);
+          if constexpr (decltype(masked)::value) {
+            a0 &= zm01;
+            a1 &= zm01;
+            a2 &= zm89;
+            a3 &= zm89;
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816(o_acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+      };
       if (part) {  // zero V rows of invalid keys (they may hold NaN)
         const int kk = key0 + 2 * c4;
-        zm01 = ((kk >= t.klo && kk <= t.khi) ? 0x0000ffffu : 0u) |
-               ((kk + 1 >= t.klo && kk + 1 <= t.khi) ? 0xffff0000u : 0u);
-        zm89 = ((kk + 8 >= t.klo && kk + 8 <= t.khi) ? 0x0000ffffu : 0u) |
-               ((kk + 9 >= t.klo && kk + 9 <= t.khi) ? 0xffff0000u : 0u);
-      }
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        const int chunk = 2 * mt + v_chi;
-        const uint32_t addr =
-            vb + (chunk >> 3) * kHalfBytes + v_row * 128 + (((chunk & 7) ^ sw) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(addr, a0, a1, a2, a3);
-        a0 &= zm01;
-        a1 &= zm01;
-        a2 &= zm89;
-        a3 &= zm89;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_16816(o_acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        const uint32_t zm01 = ((kk >= t.klo && kk <= t.khi) ? 0x0000ffffu : 0u) |
+                              ((kk + 1 >= t.klo && kk + 1 <= t.khi) ? 0xffff0000u : 0u);
+        const uint32_t zm89 = ((kk + 8 >= t.klo && kk + 8 <= t.khi) ? 0x0000ffffu : 0u) |
+                              ((kk + 9 >= t.klo && kk + 9 <= t.khi) ? 0xffff0000u : 0u);
+        pv(zm01, zm89, std::true_type{});
+      } else {
+        pv(0xffffffffu, 0xffffffffu, std::false_type{});
       }
     };
 
