@@ -142,13 +142,13 @@ struct ItemRec {
 // identically on host and device.
 struct DecodeSmem {
   int stage_bytes, stages, slot_bytes, ring_off, comb_off, pre_off, bar_off, total;
-  __host__ __device__ DecodeSmem(int D, int G, int NT, int stages_, int n_prefix) {
+  __host__ __device__ DecodeSmem(int D, int G, int NT, int stages_, int n_prefix, int comb_slots) {
     stage_bytes = 2 * (D / 64) * kHalfBytes;
     stages = stages_;
     slot_bytes = 128 + ((G * D * 2 + 127) / 128) * 128;  // item record + q rows
     ring_off = stages * stage_bytes;
     comb_off = ring_off + kItemSlots * slot_bytes;
-    const int comb_bytes = kConsumerWarps * G * (D + 4) * 4 + 2 * kConsumerWarps * 8 * NT * 4;
+    const int comb_bytes = comb_slots * G * (D + 4) * 4 + 2 * kConsumerWarps * 8 * NT * 4;
     pre_off = comb_off + ((comb_bytes + 127) / 128) * 128;
     bar_off = pre_off + ((n_prefix * 4 + 127) / 128) * 128;
     total = bar_off + (2 * stages + 2 * kItemSlots) * 8 + 16;
@@ -158,7 +158,9 @@ struct DecodeSmem {
 // MULTI: several query tokens per sequence (the rows of an item are
 // (token, head) pairs, each with its own position, mask and bias row); the
 // single-token instantiations keep the plain per-key mask.
-template <int D, int NT, int BH, bool MULTI>
+// COMB2: the item combine in two rounds through two O buffers instead of one
+// per consumer warp (the smaller buffer leaves room for a third stage).
+template <int D, int NT, int BH, bool MULTI, bool COMB2>
 __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int HALVES = D / 64;
@@ -183,12 +185,13 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   const int S = p.S;
   const int NR = p.TG * G;   // rows (token, head) of a full item
   const bool dense = S > 1;  // items enumerated through a per-sequence prefix sum
-  const DecodeSmem L(D, NR, NT, p.stages, dense ? p.B + 1 : 0);
+  constexpr int kCombSlots = COMB2 ? 2 : kConsumerWarps;
+  const DecodeSmem L(D, NR, NT, p.stages, dense ? p.B + 1 : 0, kCombSlots);
   const int stages = L.stages;
   const int STAGE_BYTES = L.stage_bytes;
 
-  float* comb_o = reinterpret_cast<float*>(smem + L.comb_off);  // [4][NR][D+4]
-  float* comb_m = comb_o + kConsumerWarps * NR * (D + 4);         // [4][HP]
+  float* comb_o = reinterpret_cast<float*>(smem + L.comb_off);  // [comb_slots][NR][D+4]
+  float* comb_m = comb_o + kCombSlots * NR * (D + 4);             // [4][HP]
   float* comb_l = comb_m + kConsumerWarps * HP;                   // [4][HP]
   int* prefix = reinterpret_cast<int*>(smem + L.pre_off);         // [B+1] items before b
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
@@ -843,36 +846,80 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         v += __shfl_xor_sync(0xffffffffu, v, 16);
         l_run[nt][j] = v;
       }
+    // Combine the four warps' (m, l, O): through one O buffer per warp, or in
+    // two rounds through two (warps 2 and 3 hand theirs to warps 0 and 1,
+    // which merge them in registers, same fragment layout), after which every
+    // thread combines the buffers.  In the merge, rows past NRi (padding) read
+    // row NRi - 1; they are never stored.
     constexpr int OP = D + 4;
-    named_bar_sync(1, kConsumerThreads);  // previous item's readers of comb_* are done
+    auto put = [&](int slot) {
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
+      for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int head = nt * 8 + 2 * c4 + (i & 1);
-          if (head < NRi) {
-            const int dim = 16 * mt + g + 8 * (i >> 1);
-            comb_o[(warp * NR + head) * OP + dim] = o_acc[mt][nt][i];
+          for (int i = 0; i < 4; ++i) {
+            const int head = nt * 8 + 2 * c4 + (i & 1);
+            if (head < NRi) {
+              const int dim = 16 * mt + g + 8 * (i >> 1);
+              comb_o[(slot * NR + head) * OP + dim] = o_acc[mt][nt][i];
+            }
           }
-        }
-    if (g == 0) {
+      if (g == 0) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int head = nt * 8 + 2 * c4 + j;
-          comb_m[warp * HP + head] = m_run[nt][j];
-          comb_l[warp * HP + head] = l_run[nt][j];
-        }
+          for (int j = 0; j < 2; ++j) {
+            const int head = nt * 8 + 2 * c4 + j;
+            comb_m[slot * HP + head] = m_run[nt][j];
+            comb_l[slot * HP + head] = l_run[nt][j];
+          }
+      }
+    };
+    named_bar_sync(1, kConsumerThreads);  // previous item's readers of comb_* are done
+    if constexpr (!COMB2) {
+      put(warp);
+    } else {
+      if (warp >= 2) put(warp - 2);
+      named_bar_sync(1, kConsumerThreads);
+      if (warp < 2) {
+        float sa[NT][2], sb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            int head = nt * 8 + 2 * c4 + j;
+            head = head < NRi ? head : NRi - 1;
+            const float mo = comb_m[warp * HP + head], lo = comb_l[warp * HP + head];
+            const float mx = fmaxf(m_run[nt][j], mo);
+            const float base = mx == -INFINITY ? 0.f : mx;
+            sa[nt][j] = ex2(m_run[nt][j] - base);
+            sb[nt][j] = ex2(mo - base);
+            l_run[nt][j] = fmaf(sa[nt][j], l_run[nt][j], sb[nt][j] * lo);
+            m_run[nt][j] = mx;
+          }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              int head = nt * 8 + 2 * c4 + (i & 1);
+              head = head < NRi ? head : NRi - 1;
+              const int dim = 16 * mt + g + 8 * (i >> 1);
+              o_acc[mt][nt][i] = fmaf(sa[nt][i & 1], o_acc[mt][nt][i],
+                                      sb[nt][i & 1] * comb_o[(warp * NR + head) * OP + dim]);
+            }
+      }
+      named_bar_sync(1, kConsumerThreads);  // warps 2 and 3's partials are consumed
+      if (warp < 2) put(warp);
     }
     named_bar_sync(1, kConsumerThreads);
     for (int i = tid; i < NRi * D; i += kConsumerThreads) {
       const int h = i / D, d = i - h * D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * HP + h]);
+      for (int w = 0; w < kCombSlots; ++w) M = fmaxf(M, comb_m[w * HP + h]);
       float Ls = 0.f, o = 0.f;
       // MULTI, M = -inf: no key of this item is visible to the row (a split
       // may lie wholly past a row's position): an empty result, o = 0 and
@@ -880,7 +927,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       // of an item is visible to its rows.
       if (!MULTI || M > -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < kCombSlots; ++w) {
           const float sc = ex2(comb_m[w * HP + h] - M);
           Ls = fmaf(sc, comb_l[w * HP + h], Ls);
           o = fmaf(sc, comb_o[(w * NR + h) * OP + d], o);
@@ -977,9 +1024,9 @@ static int sm_count() {
   return n;
 }
 
-template <int D, int NT, int BH, bool MULTI>
+template <int D, int NT, int BH, bool MULTI, bool COMB2 = false>
 static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int smem_bytes, int grid) {
-  auto kern = decode_kernel<D, NT, BH, MULTI>;
+  auto kern = decode_kernel<D, NT, BH, MULTI, COMB2>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -1045,9 +1092,19 @@ int launch_decode(const DecodeCall& c) {
   // kCtasPerSm CTAs per SM: keep each CTA under the budget; 2..max stages
   const int budget = INKLING_DECODE_SMEM_BUDGET_KB * 1024;
   int stages = INKLING_DECODE_MAX_STAGES;
-  while (stages > 2 && DecodeSmem(c.D, NR, NT, stages, n_prefix).total > budget) --stages;
+  // The item combine takes one O buffer per consumer warp, or half as many in
+  // two rounds (warps 2, 3 hand theirs to warps 0, 1): the two-round combine
+  // costs per-item latency, so it is used only where it makes room for a
+  // third stage -- which happens only for D = 128 with one n-tile (rows 5..8).
+  const auto fits3 = [&](int slots) {
+    return DecodeSmem(c.D, NR, NT, 3, n_prefix, slots).total <= budget;
+  };
+  const bool comb2 = c.D == 128 && NT == 1 && !fits3(kConsumerWarps) && fits3(2);
+  const int comb_slots = comb2 ? 2 : kConsumerWarps;
+  while (stages > 2 && DecodeSmem(c.D, NR, NT, stages, n_prefix, comb_slots).total > budget)
+    --stages;
   prm.stages = stages;
-  const int smem = 1024 + DecodeSmem(c.D, NR, NT, stages, n_prefix).total;
+  const int smem = 1024 + DecodeSmem(c.D, NR, NT, stages, n_prefix, comb_slots).total;
   if (smem > 227 * 1024) return INKLING_ERR_ARG;  // batch too large for the item prefix table
 
   // Static schedule (one split per sequence): give every CTA the same number
@@ -1068,10 +1125,12 @@ int launch_decode(const DecodeCall& c) {
   if (QL == 1) {
     if (c.D == 128) {
       if (BH == 64)
-        rc = NT == 1 ? launch_decode_t<128, 1, 64, false>(c, prm, smem, grid)
+        rc = NT == 1 ? (comb2 ? launch_decode_t<128, 1, 64, false, true>(c, prm, smem, grid)
+                              : launch_decode_t<128, 1, 64, false>(c, prm, smem, grid))
                      : launch_decode_t<128, 2, 64, false>(c, prm, smem, grid);
       else
-        rc = NT == 1 ? launch_decode_t<128, 1, 16, false>(c, prm, smem, grid)
+        rc = NT == 1 ? (comb2 ? launch_decode_t<128, 1, 16, false, true>(c, prm, smem, grid)
+                              : launch_decode_t<128, 1, 16, false>(c, prm, smem, grid))
                      : launch_decode_t<128, 2, 16, false>(c, prm, smem, grid);
     } else {
       if (BH == 64)
@@ -1084,10 +1143,12 @@ int launch_decode(const DecodeCall& c) {
   } else {
     if (c.D == 128) {
       if (BH == 64)
-        rc = NT == 1 ? launch_decode_t<128, 1, 64, true>(c, prm, smem, grid)
+        rc = NT == 1 ? (comb2 ? launch_decode_t<128, 1, 64, true, true>(c, prm, smem, grid)
+                              : launch_decode_t<128, 1, 64, true>(c, prm, smem, grid))
                      : launch_decode_t<128, 2, 64, true>(c, prm, smem, grid);
       else
-        rc = NT == 1 ? launch_decode_t<128, 1, 16, true>(c, prm, smem, grid)
+        rc = NT == 1 ? (comb2 ? launch_decode_t<128, 1, 16, true, true>(c, prm, smem, grid)
+                              : launch_decode_t<128, 1, 16, true>(c, prm, smem, grid))
                      : launch_decode_t<128, 2, 16, true>(c, prm, smem, grid);
     } else {
       if (BH == 64)
