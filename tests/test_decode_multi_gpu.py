@@ -74,6 +74,19 @@ def test_forced_splits(ops, splits):
     assert_close(out, ro, lse, rl, what=f"{splits} splits")
 
 
+@pytest.mark.parametrize("case,splits", [(1, 3), (1, 7), (2, 2)])
+def test_forced_splits_six_rows(ops, case, splits):
+    """Token groups of 2 tokens x 3 heads (six rows, D = 128: the two-round
+    item combine) over splits of long causal ranges; an early group sees
+    fewer keys than the last, so a split can be empty for it."""
+    lens, ql, H_q, H_kv, D, P, win, R = CASES[case]
+    inp = make(lens, ql, H_q, H_kv, D, P, win, R, seed=370 + 10 * case + splits)
+    out, lse, err = run(ops, inp, ql, num_splits=splits)
+    assert err == 0
+    ro, rl, _ = oracle_prefill(inp)
+    assert_close(out, ro, lse, rl, what=f"case {case}, {splits} splits")
+
+
 def test_one_token_is_decode_bit_exact(ops):
     inp = W.make_decode(6, 48, 16, 128, 64, [1, 63, 64, 65, 700, 3000], 512, 512, device=DEV,
                         seed=21)
