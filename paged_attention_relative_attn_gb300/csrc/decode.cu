@@ -21,14 +21,17 @@
 //    the next item's K/V stream in while the consumers finish the current one.
 //  * four consumer warps that each own 16 rows of every tile and compute the
 //    transposed products S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16
-//    (the GQA group of <= 8 query heads is the N = 8 side, so M is never
-//    padded), add the bias from a shared-memory copy of the needed slice of
-//    rel_logits (pre-multiplied by log2 e), mask, and keep an online softmax
-//    per head with warp shuffles over the keys.  P goes from the accumulator
-//    layout to the B-operand layout with movmatrix.  At the end of an item the
-//    four warps' (m, l, O) are combined through shared memory and written as
-//    the final bf16 output or, when the sequence spans several splits, as a
-//    normalised fp32 partial plus its lse for the merge kernel.
+//    (the rows of an item -- the GQA group's query heads, or (token, head)
+//    pairs of a token group for multi-token decode -- are the N side, one or
+//    two 8-wide n-tiles, so M is never padded), add the bias read from L2
+//    (the producer prefetches each item's rel_logits rows there; each tile's
+//    values are loaded one tile ahead), mask, and keep an online softmax per
+//    row with warp shuffles over the keys.  P goes from the accumulator layout
+//    to the B-operand layout with movmatrix.  At the end of an item the four
+//    warps' (m, l, O) are combined through shared memory (one buffer per warp,
+//    or two buffers in two rounds where that leaves room for a third stage)
+//    and written as the final bf16 output or, when the sequence spans several
+//    splits, as a normalised fp32 partial plus its lse for the merge kernel.
 // Reduction order depends only on logical key positions and host scalars,
 // never on page ids or on which CTA ran an item, so results are bit-identical
 // under any physical page permutation and any schedule.

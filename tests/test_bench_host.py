@@ -66,3 +66,26 @@ def test_packed_sizes_of_the_local_decode_step():
              (torch.int32, (64, 128)), (torch.int32, (64,))]
     exact = 64 * 48 * 128 * 2 + 64 * 48 * 512 * 4 + 64 * 128 * 4 + 64 * 4
     assert bench._packed_bytes(specs) == exact == 7110912
+
+
+def test_source_hash_ignores_comments_and_layout(tmp_path, monkeypatch):
+    code = 'int f(int x) {\n  return x + 1;  // one\n}\nconst char* s = "// kept /* too */";\n'
+    edited = '/* header */\nint f(int x) {\n    return x + 1;\n}\n// note\nconst char* s = "// kept /* too */";\n'
+    changed = code.replace("x + 1", "x + 2")
+    for name, text in (("a.cu", code), ("b.cu", edited), ("c.cu", changed)):
+        (tmp_path / name).write_text(text)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.source_hash(["a.cu"]) == bench.source_hash(["b.cu"])
+    assert bench.source_hash(["a.cu"]) != bench.source_hash(["c.cu"])
+    assert '"// kept /* too */"' in bench.strip_c_comments(code)
+
+
+def test_traffic_records_match_the_current_sources():
+    """Every committed DRAM-traffic record was taken on the kernel code as it
+    stands (a stale record would make the bench report traffic null)."""
+    import json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        recs = json.load(f)
+    for key, rec in recs.items():
+        kernel = key.split(":")[0]
+        assert rec["source_hash"] == bench.source_hash(bench.KERNEL_SOURCES[kernel]), key
