@@ -143,29 +143,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   const int qt = blockIdx.y - b * p.tiles_per_seq;
   if (b >= p.B) return;
 
-  // ---- the query tile and its key range (identical in every thread)
-  const int tb = p.cu_seqlens_q[b];
-  const int q_len = p.cu_seqlens_q[b + 1] - tb;
-  if (q_len <= 0 || qt * kQRows >= q_len) return;
-  int L = p.seq_lens[b];
-  const int cap = p.pt_stride * p.P;
-  if (L > cap) {
-    if (tid == 0 && h == 0 && qt == 0) report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
-    L = cap;
-  }
-  if (q_len > L || tb < 0 || tb + q_len > p.T) {
-    if (tid == 0 && h == 0 && qt == 0) report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);
-    return;
-  }
-  if (q_len > p.max_q_len && tid == 0 && h == 0 && qt == 0)
-    report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);  // tiles past the grid are not computed
-  const int t0 = tb + qt * kQRows;
-  const int nrows = min(kQRows, q_len - qt * kQRows);
-  const int pos0 = L - q_len + qt * kQRows;  // position of row 0
-  const int khi_all = pos0 + nrows - 1;
-  const int klo_all = p.window > 0 ? max(0, pos0 - p.window + 1) : 0;
-  const int hkv = h / p.G;
-  const int R = p.R;
+  // ---- the sequence's scalars, loaded together; their latency overlaps the
+  // barrier and TMEM set-up below, and nothing reads them before it
+  const int tb = __ldg(p.cu_seqlens_q + b);
+  const int te = __ldg(p.cu_seqlens_q + b + 1);
+  const int L_in = __ldg(p.seq_lens + b);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::BAR_OFF);
   uint64_t* q_full = bars;
@@ -219,6 +201,36 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // ---- the query tile and its key range (identical in every thread); a CTA
+  // with nothing to do frees its TMEM and leaves
+  const int q_len = te - tb;
+  int L = L_in;
+  bool run = q_len > 0 && qt * kQRows < q_len;
+  if (run) {
+    const int cap = p.pt_stride * p.P;
+    if (L > cap) {
+      if (tid == 0 && h == 0 && qt == 0) report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
+      L = cap;
+    }
+    if (q_len > L || tb < 0 || tb + q_len > p.T) {
+      if (tid == 0 && h == 0 && qt == 0) report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);
+      run = false;
+    } else if (q_len > p.max_q_len && tid == 0 && h == 0 && qt == 0) {
+      report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);  // tiles past the grid are not computed
+    }
+  }
+  if (!run) {
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  const int t0 = tb + qt * kQRows;
+  const int nrows = min(kQRows, q_len - qt * kQRows);
+  const int pos0 = L - q_len + qt * kQRows;  // position of row 0
+  const int khi_all = pos0 + nrows - 1;
+  const int klo_all = p.window > 0 ? max(0, pos0 - p.window + 1) : 0;
+  const int hkv = h / p.G;
+  const int R = p.R;
 
   // =================================================================== loaders
   if (warp == 0 || warp == 6) {
