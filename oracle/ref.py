@@ -44,7 +44,10 @@ Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, textbook SDPA, shift invariance, single key,
 one-hot bias, window immunity, page permutation, clamp expansion; for the KV
 append a hand-worked example and a read-back through the pinned gather of
-values that encode each token's position).
+values that encode each token's position; for the short convolution a
+hand-worked example, the impulse response, ``numpy.convolve``, invariance
+under how a sequence is cut into chunks, and width 1 reducing to the plain
+append).
 """
 
 from __future__ import annotations
@@ -64,6 +67,10 @@ __all__ = [
     "token_positions",
     "cache_slot",
     "ref_kv_append",
+    "conv_tap_offset",
+    "conv_input",
+    "short_conv_chunk",
+    "ref_kv_conv_append",
 ]
 
 
@@ -278,3 +285,100 @@ def ref_kv_append(k_cache, v_cache, page_table, cu_seqlens_q, seq_lens, k_new, v
             kc[page, slot] = k_new[t]
             vc[page, slot] = v_new[t]
     return kc, vc
+
+
+# --------------------------------------------------------------------------
+# Causal short convolution on K and V, ahead of the KV append
+# --------------------------------------------------------------------------
+#
+# TensorRT-LLM PR #17062, "Architecture": each layer has four causal short
+# convolutions, two of them inside attention (on K and on V), and they carry
+# per-request state across decode steps; "pyexecutor" row: that state lives in
+# a pool with one row per request.  The pages give neither the width nor the
+# layout, so the plainest reading is taken and the width is a parameter:
+#
+#   * depthwise over the H_kv * D channels of a token's K (resp. V) row, along
+#     the token axis, no bias, no activation;
+#   * weight[c, j], j = 0 .. w-1: tap j multiplies the input w-1-j tokens back
+#     (tap w-1 multiplies the current token):
+#         y_t[c] = sum_j weight[c, j] * x_{t-(w-1)+j}[c]
+#   * a request's state is its last w-1 inputs (pre-convolution rows), oldest
+#     first; a new request's state is zero;
+#   * the convolved rows y are what the cache holds (the convolution runs ahead
+#     of the append, inside attention).
+
+
+def conv_tap_offset(j: int, w: int) -> int:
+    """Token offset of tap ``j`` of a width-``w`` causal convolution: it
+    multiplies the input ``w - 1 - j`` tokens before the current one."""
+    return j - (w - 1)
+
+
+def conv_input(x_chunk: np.ndarray, state: np.ndarray, r: int) -> np.ndarray:
+    """Input row at chunk-relative index ``r``: the chunk's own row when
+    ``r >= 0``, else row ``(w - 1) + r`` of the request's state (its previous
+    ``w - 1`` inputs, oldest first)."""
+    return x_chunk[r] if r >= 0 else state[state.shape[0] + r]
+
+
+def short_conv_chunk(x_chunk, state, weight):
+    """One request's new inputs through the causal short convolution.
+
+    x_chunk [n, C] (oldest first), state [w-1, C], weight [C, w].  Returns
+    (y [n, C], new_state [w-1, C]): y_i = sum_j weight[:, j] * input at
+    i + conv_tap_offset(j, w); the new state is the last w-1 inputs, which
+    reach back into the old state when n < w-1.
+    """
+    x_chunk = np.asarray(x_chunk, dtype=np.float64)
+    state = np.asarray(state, dtype=np.float64)
+    weight = np.asarray(weight, dtype=np.float64)
+    n, C = x_chunk.shape
+    w = weight.shape[1]
+    y = np.zeros((n, C))
+    for i in range(n):
+        for j in range(w):
+            y[i] += weight[:, j] * conv_input(x_chunk, state, i + conv_tap_offset(j, w))
+    new_state = np.zeros((w - 1, C))
+    for j in range(w - 1):
+        new_state[j] = conv_input(x_chunk, state, n - (w - 1) + j)
+    return y, new_state
+
+
+def ref_kv_conv_append(k_cache, v_cache, page_table, cu_seqlens_q, seq_lens, k_new, v_new,
+                       w_k, w_v, state_k, state_v, state_slots):
+    """The short convolutions on K and V of each request's new tokens, then
+    the KV append of the convolved rows (see the reading above; the append is
+    ``ref_kv_append``'s placement: token t of sequence b at position p goes to
+    ``page_table[b, p // P]``, slot ``p % P``).
+
+    k/v_cache [num_pages, P, H_kv, D]; k/v_new [T, H_kv, D]; w_k/w_v
+    [H_kv, D, w]; state_k/v [num_slots, w-1, H_kv, D]; state_slots [B], the
+    pool row of each sequence (distinct).  Returns new float64 arrays
+    (k_cache, v_cache, state_k, state_v); the inputs are not modified.
+    """
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    sk = np.array(state_k, dtype=np.float64, copy=True)
+    sv = np.array(state_v, dtype=np.float64, copy=True)
+    pt = np.asarray(page_table, dtype=np.int64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    P = kc.shape[1]
+    H, D = kc.shape[2], kc.shape[3]
+    C = H * D
+    w = np.asarray(w_k).shape[2]
+    pos = token_positions(cu_seqlens_q, seq_lens)
+    for b in range(len(cu) - 1):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        slot = int(state_slots[b])
+        outs = []
+        for x_new, wt, st in ((k_new, w_k, sk), (v_new, w_v, sv)):
+            x = np.asarray(x_new, dtype=np.float64)[t0:t1].reshape(t1 - t0, C)
+            y, new_st = short_conv_chunk(x, st[slot].reshape(w - 1, C),
+                                         np.asarray(wt, dtype=np.float64).reshape(C, w))
+            st[slot] = new_st.reshape(w - 1, H, D)
+            outs.append(y.reshape(t1 - t0, H, D))
+        for i, t in enumerate(range(t0, t1)):
+            page, s = cache_slot(pt[b], int(pos[t]), P)
+            kc[page, s] = outs[0][i]
+            vc[page, s] = outs[1][i]
+    return kc, vc, sk, sv

@@ -354,11 +354,107 @@ def pin_kv_append_readback(R=ref):
     assert int(np.isnan(kc[:, :, 0, 0]).sum()) == pool * P - sum(lens)
 
 
+def pin_conv_hand(R=ref):
+    """Worked by hand, one channel, width 3, taps (0.25, 0.5, 1.0) from the
+    oldest input to the current one, state (2, 4):
+      chunk (8, 16): y = 0.25*2 + 0.5*4 + 8 = 10.5 and 0.25*4 + 0.5*8 + 16 = 21,
+                     new state (8, 16);
+      chunk (8):     y = 10.5, new state (4, 8) -- half old state, half new.
+    Through the paged append: P = 4, pages [2, 0], 6 tokens of which the last
+    2 are new (positions 4, 5 -> page 0 slots 0, 1), state in pool row 1."""
+    wgt = np.array([[0.25, 0.5, 1.0]])
+    y, st = R.short_conv_chunk(np.array([[8.0], [16.0]]), np.array([[2.0], [4.0]]), wgt)
+    assert np.array_equal(y.ravel(), [10.5, 21.0]) and np.array_equal(st.ravel(), [8.0, 16.0])
+    y, st = R.short_conv_chunk(np.array([[8.0]]), np.array([[2.0], [4.0]]), wgt)
+    assert np.array_equal(y.ravel(), [10.5]) and np.array_equal(st.ravel(), [4.0, 8.0])
+    kc = np.zeros((3, 4, 1, 1))
+    state = np.zeros((2, 2, 1, 1))
+    state[1, :, 0, 0] = [2.0, 4.0]
+    k_new = np.array([8.0, 16.0]).reshape(2, 1, 1)
+    wk = wgt.reshape(1, 1, 3)
+    k2, v2, sk, sv = R.ref_kv_conv_append(kc, kc, np.array([[2, 0]]), np.array([0, 2]),
+                                          np.array([6]), k_new, -k_new, wk, 2 * wk,
+                                          state, -state, np.array([1]))
+    expect = np.zeros((3, 4, 1, 1))
+    expect[0, 0], expect[0, 1] = 10.5, 21.0
+    assert np.array_equal(k2, expect) and np.array_equal(v2, -2 * expect)
+    assert np.array_equal(sk[1, :, 0, 0], [8.0, 16.0]) and np.array_equal(sv[1, :, 0, 0], [-8.0, -16.0])
+    assert np.array_equal(sk[0], np.zeros((2, 1, 1)))  # other pool rows untouched
+
+
+def pin_conv_impulse_response(R=ref):
+    """A unit impulse at token 2 (zero state) returns the taps newest first:
+    y_{2+k} = weight[:, w-1-k], and zero elsewhere."""
+    rng = np.random.default_rng(5)
+    C, w, n = 3, 4, 9
+    wgt = rng.normal(size=(C, w))
+    x = np.zeros((n, C))
+    x[2] = 1.0
+    y, _ = R.short_conv_chunk(x, np.zeros((w - 1, C)), wgt)
+    want = np.zeros((n, C))
+    for k in range(w):
+        want[2 + k] = wgt[:, w - 1 - k]
+    assert np.array_equal(y, want)
+
+
+def pin_conv_numpy_convolve(R=ref):
+    """Each channel equals numpy.convolve of (state, chunk) with the reversed
+    taps, 'valid' part; the new state is the last w-1 inputs."""
+    rng = np.random.default_rng(6)
+    C, w, n = 5, 4, 7
+    wgt, st, x = rng.normal(size=(C, w)), rng.normal(size=(w - 1, C)), rng.normal(size=(n, C))
+    y, new_st = R.short_conv_chunk(x, st, wgt)
+    a = np.concatenate([st, x])
+    for c in range(C):
+        np.testing.assert_allclose(y[:, c], np.convolve(a[:, c], wgt[c, ::-1], mode="valid"),
+                                   rtol=0, atol=1e-12)
+    assert np.array_equal(new_st, a[-(w - 1):])
+
+
+def pin_conv_chunking_invariance(R=ref):
+    """Cutting a sequence into chunks (3 + 1 + 6 tokens, the state carried
+    between calls) gives exactly the outputs and final state of one call."""
+    rng = np.random.default_rng(7)
+    C, w, n = 4, 4, 10
+    wgt, x = rng.normal(size=(C, w)), rng.normal(size=(n, C))
+    y_all, st_all = R.short_conv_chunk(x, np.zeros((w - 1, C)), wgt)
+    st, parts, lo = np.zeros((w - 1, C)), [], 0
+    for m in (3, 1, 6):
+        y, st = R.short_conv_chunk(x[lo:lo + m], st, wgt)
+        parts.append(y)
+        lo += m
+    assert np.array_equal(np.concatenate(parts), y_all) and np.array_equal(st, st_all)
+
+
+def pin_conv_width1_is_append(R=ref):
+    """Width 1 with unit taps is the identity: the convolved append equals
+    the (separately pinned) plain append."""
+    lens, q_lens, P, H, D = [9, 1, 17], [3, 1, 5], 4, 2, 3
+    gc = torch.Generator().manual_seed(8)
+    max_pages = max(W.pages_for(L, P) for L in lens)
+    pool = sum(W.pages_for(L, P) for L in lens) + 1
+    pt, _ = W.build_page_table(lens, P, max_pages, pool, gc)
+    pt = npi(pt)
+    rng = np.random.default_rng(8)
+    kc, vc = rng.normal(size=(pool, P, H, D)), rng.normal(size=(pool, P, H, D))
+    T = sum(q_lens)
+    k_new, v_new = rng.normal(size=(T, H, D)), rng.normal(size=(T, H, D))
+    cu = np.concatenate([[0], np.cumsum(q_lens)])
+    ones = np.ones((H, D, 1))
+    st = np.zeros((3, 0, H, D))
+    k2, v2, _, _ = R.ref_kv_conv_append(kc, vc, pt, cu, lens, k_new, v_new, ones, ones, st, st,
+                                        np.array([2, 0, 1]))
+    k3, v3 = R.ref_kv_append(kc, vc, pt, cu, lens, k_new, v_new)
+    assert np.array_equal(k2, k3) and np.array_equal(v2, v3)
+
+
 ALL_PINS = [pin_brute_tiny_decode, pin_brute_small_decode, pin_brute_small_prefill,
             pin_zero_bias_is_sdpa, pin_constant_bias_shift, pin_single_visible_key,
             pin_one_hot_bias, pin_window_immunity, pin_page_permutation,
             pin_clamp_expansion, pin_closed_form, pin_decode_is_last_prefill_token,
-            pin_empty_sequence, pin_kv_append_hand, pin_kv_append_readback]
+            pin_empty_sequence, pin_kv_append_hand, pin_kv_append_readback,
+            pin_conv_hand, pin_conv_impulse_response, pin_conv_numpy_convolve,
+            pin_conv_chunking_invariance, pin_conv_width1_is_append]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -380,6 +476,10 @@ MUTANTS = {
         [[int(s[b]) - int(c[b + 1] - c[b]) + i + 1 for i in range(int(c[b + 1] - c[b]))]
          for b in range(len(s))] + [[]]).astype(np.int64))(np.asarray(cu), np.asarray(sl))),
     "append_slot_transposed": ("cache_slot", lambda row, p, P: (int(row[p // P]), (p // P) % P)),
+    "conv_taps_reversed": ("conv_tap_offset", lambda j, w: -j),
+    "conv_state_newest_first": ("conv_input", lambda x, st, r: x[r] if r >= 0 else st[-r - 1]),
+    "conv_state_off_by_one": ("conv_input",
+                              lambda x, st, r: x[r] if r >= 0 else st[max(st.shape[0] + r - 1, 0)]),
 }
 
 
