@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload local_decode|global_decode|chunked_prefill|global_prefill|
-                                kv_append|mtp_decode|decode_66_layers]
+                                kv_append|kv_conv_append|mtp_decode|decode_66_layers]
                     [--no-cpu-baseline] [--no-e2e] [--no-extra] [--batch B] [--sets S]
 
 Prints ONE JSON line (rank 0).  The default workload is the local-layer decode
@@ -461,6 +461,52 @@ def bench_kv_append(args, device, K, warmup):
                 unit="GB/s")
 
 
+def bench_kv_conv_append(args, device, K, warmup):
+    """One step = the short convolutions on K and V (width 4) ahead of the
+    KV append, for one chunked-prefill call: the same 4 sequences x 2048 new
+    tokens as ``kv_append``, c cycling over the four calls; each sequence has
+    its own state pool row.  Bytes: every new K and V row read once and every
+    convolved row written once, plus the state rows read and rewritten and the
+    taps."""
+    import paged_attention_relative_attn_gb300 as ira
+    cfg = W.CHUNKED_PREFILL
+    width = 4
+    n = cfg["n_seqs"] if args.batch is None else args.batch
+    chunk, L = cfg["chunk"], cfg["seq_len"]
+    H, D = cfg["H_kv"], cfg["D"]
+    cache = W.make_prefill_cache([L] * n, H, D, cfg["P"], device=device, seed=0)
+    g = torch.Generator(device=device).manual_seed(6)
+    T = n * chunk
+    cu = (torch.arange(n + 1, dtype=torch.int32) * chunk).to(device)
+    w_k = 0.5 * torch.randn((H, D, width), generator=g, device=device)
+    w_v = 0.5 * torch.randn((H, D, width), generator=g, device=device)
+    s_k = torch.randn((n, width - 1, H, D), generator=g, device=device).to(torch.bfloat16)
+    s_v = torch.randn((n, width - 1, H, D), generator=g, device=device).to(torch.bfloat16)
+    slots = torch.arange(n, dtype=torch.int32, device=device)
+    calls = []
+    for c in range(4):
+        k_new = torch.randn((T, H, D), generator=g, device=device).to(torch.bfloat16)
+        v_new = torch.randn((T, H, D), generator=g, device=device).to(torch.bfloat16)
+        sl = torch.full((n,), chunk * (c + 1), dtype=torch.int32, device=device)
+        calls.append((k_new, v_new, sl))
+    per_call = (2 * 2 * T * H * D * 2            # new rows read, convolved rows written
+                + 2 * 2 * n * (width - 1) * H * D * 2  # state rows read and rewritten
+                + 2 * H * D * width * 4)          # taps
+
+    def step(i, stream):
+        k_new, v_new, sl = calls[i % 4]
+        ira.kv_conv_append(k_new, v_new, cu, sl, cache.page_table, cache.k_cache, cache.v_cache,
+                           w_k, w_v, s_k, s_v, slots, max_q_len=chunk, stream=stream)
+
+    ms, clocks = time_steps(args, device, step, K, warmup, 40)
+    config = {"workload": "kv_conv_append", "sequences": n, "tokens_per_call": T, "width": width,
+              "heads_kv": H, "head_dim": D, "page_size": cfg["P"],
+              "l2": f"4 calls x {per_call / 1e6:.0f} MB per rotation (L2 129 MB)"}
+    return dict(ms=ms, K=K, clocks=clocks, launches=K, config=config, units_total=K * per_call,
+                bytes_total=K * per_call, kernel="kv_conv_append_kernel", kernel_launches=K,
+                unit="GB/s")
+
+
 def bench_stack(args, device, K, warmup):
     """One step = one decode step over the 66-layer stack: 55 local layers
     (16 KV heads, window 512, R=512) and 11 global layers (8 KV heads, full
@@ -736,11 +782,13 @@ def run_reference(args):
 
 
 DEFAULT_STEPS = {"local_decode": 10000, "global_decode": 2000, "chunked_prefill": 200,
-                 "global_prefill": 50, "kv_append": 2000, "mtp_decode": 5000,
-                 "decode_66_layers": 40}
+                 "global_prefill": 50, "kv_append": 2000, "kv_conv_append": 2000,
+                 "mtp_decode": 5000, "decode_66_layers": 40}
 KERNEL_SOURCES = {
     "kv_append_kernel": ["paged_attention_relative_attn_gb300/csrc/kv_append.cu",
                          "paged_attention_relative_attn_gb300/csrc/plan.cuh"],
+    "kv_conv_append_kernel": ["paged_attention_relative_attn_gb300/csrc/kv_conv.cu",
+                              "paged_attention_relative_attn_gb300/csrc/plan.cuh"],
     "decode_kernel": ["paged_attention_relative_attn_gb300/csrc/decode.cu",
                       "paged_attention_relative_attn_gb300/csrc/plan.cuh",
                       "paged_attention_relative_attn_gb300/csrc/ptx.cuh"],
@@ -758,6 +806,8 @@ def run_workload(args, device, name, K, warmup):
         return bench_prefill(args, device, K, warmup, name)
     if name == "kv_append":
         return bench_kv_append(args, device, K, warmup)
+    if name == "kv_conv_append":
+        return bench_kv_conv_append(args, device, K, warmup)
     if name == "mtp_decode":
         return bench_decode_multi(args, device, K, warmup)
     return bench_stack(args, device, K, warmup)
@@ -813,7 +863,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="local_decode",
                     choices=["local_decode", "global_decode", "chunked_prefill",
-                             "global_prefill", "kv_append", "mtp_decode", "decode_66_layers"])
+                             "global_prefill", "kv_append", "kv_conv_append", "mtp_decode",
+                             "decode_66_layers"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=5.0)
@@ -872,7 +923,8 @@ def main():
     if not args.no_extra and args.workload == "local_decode":
         extra = {}
         for name, K in (("global_decode", 1000), ("chunked_prefill", 100),
-                        ("global_prefill", 20), ("kv_append", 1000), ("mtp_decode", 2000),
+                        ("global_prefill", 20), ("kv_append", 1000), ("kv_conv_append", 1000),
+                        ("mtp_decode", 2000),
                         ("decode_66_layers", 20)):
             rr = run_workload(args, device, name, K, 5)
             extra[name] = summarize(args, rr, pk)

@@ -66,6 +66,7 @@ extern "C" {
 #define INKLING_DEVERR_SEQ_TOO_LONG 2 /* seq_len > page_table_stride*page_size (clamped) */
 #define INKLING_DEVERR_TIMEOUT 4     /* a pipeline wait gave up; outputs are invalid */
 #define INKLING_DEVERR_BAD_CHUNK 8   /* prefill: q_len > seq_len or q_len > max_q_len */
+#define INKLING_DEVERR_BAD_SLOT 16   /* kv_conv_append: state pool row out of range */
 
 /*
  * inkling_rel_attn_decode -- one query token per sequence.
@@ -242,6 +243,61 @@ int inkling_rel_attn_kv_append(
     int32_t page_table_stride, int32_t B, int32_t T, int32_t H_kv, int32_t D,
     int32_t page_size, int32_t num_pages, void* k_cache, void* v_cache,
     int32_t* device_error, void* stream);
+
+/*
+ * inkling_rel_attn_kv_conv_append -- the causal short convolutions on K and V
+ * of the new tokens, then the KV append of the convolved rows (TensorRT-LLM
+ * PR #17062, "Architecture": two causal short convolutions inside attention,
+ * on K and on V, carrying per-request state across decode steps;
+ * "pyexecutor" row: the state lives in a pool with one row per request).
+ *
+ * The pages give no width, layout, bias or activation; this is the plainest
+ * form: depthwise over the C = H_kv * D channels of a token's row, causal
+ * along the tokens, no bias, no activation.  For channel c of token i of
+ * sequence b (tokens numbered as in inkling_rel_attn_kv_append):
+ *
+ *   y_i[c] = sum_{j=0}^{width-1} w[c * width + j] * x_{i-(width-1)+j}[c]
+ *
+ * (tap width-1 multiplies the current token) where the inputs before the
+ * sequence's new tokens are the rows of its state, state[state_slots[b]]: its
+ * last width-1 inputs, oldest first (zeros for a new request).  y (rounded to
+ * bf16, fp32 accumulation) goes to the cache slot of the token's position, as
+ * inkling_rel_attn_kv_append places rows; afterwards the state row holds the
+ * sequence's last width-1 inputs (raw, not convolved).  K and V have their own
+ * taps and states.
+ *
+ *   k_new, v_new      bf16 [T, H_kv, D] (device), 16-byte aligned
+ *   conv_w_k, conv_w_v fp32 [H_kv, D, width] (device)
+ *   width             1 .. 8 (1: no state; the state pointers may be NULL)
+ *   conv_state_k, conv_state_v bf16 [num_slots, width - 1, H_kv, D] (device),
+ *                     16-byte aligned, read and rewritten in place
+ *   state_slots       int32 [B] (device): the pool row of each sequence; rows
+ *                     must be distinct within a call
+ *   cu_seqlens_q, seq_lens, page_table, k_cache, v_cache: as for
+ *                     inkling_rel_attn_kv_append
+ *   max_q_len         host bound on the new tokens of one sequence (the grid
+ *                     covers max_q_len tokens per sequence)
+ * The caller owns every buffer; nothing is allocated or synchronised, and the
+ * call can be captured in a CUDA graph.  Returns INKLING_OK or a negative
+ * INKLING_ERR_* code after host checks (width, D in {64, 128}, page_size,
+ * positive pool / stride / num_slots, alignment, B * ceil(max_q_len / 32) <=
+ * 65535).  On the device: an
+ * inconsistent chunk (q_len_b > seq_lens[b]) sets INKLING_DEVERR_BAD_CHUNK and
+ * the sequence is skipped; q_len_b > max_q_len sets it too and the tokens past
+ * max_q_len are not written; a state row outside [0, num_slots) sets
+ * INKLING_DEVERR_BAD_SLOT and the sequence is skipped; positions past the
+ * page-table row and bad page ids set INKLING_DEVERR_SEQ_TOO_LONG /
+ * INKLING_DEVERR_BAD_PAGE and those rows are not written.
+ */
+int inkling_rel_attn_kv_conv_append(
+    const void* k_new, const void* v_new, const int32_t* cu_seqlens_q,
+    const int32_t* seq_lens, const int32_t* page_table,
+    int32_t page_table_stride, const float* conv_w_k, const float* conv_w_v,
+    int32_t width, void* conv_state_k, void* conv_state_v,
+    const int32_t* state_slots, int32_t num_slots, int32_t B, int32_t T,
+    int32_t max_q_len, int32_t H_kv, int32_t D, int32_t page_size,
+    int32_t num_pages, void* k_cache, void* v_cache, int32_t* device_error,
+    void* stream);
 
 /*
  * inkling_rel_attn_choose_splits -- the decode split count, a pure host

@@ -14,10 +14,11 @@ from .ops import (  # noqa: F401
     decode_multi_workspace_bytes,
     decode_workspace_bytes,
     kv_append,
+    kv_conv_append,
     prefill,
     prefill_inputs,
 )
 
 __all__ = ["InklingError", "choose_splits", "decode", "decode_inputs", "decode_multi",
            "decode_multi_workspace_bytes", "decode_workspace_bytes",
-           "kv_append", "prefill", "prefill_inputs"]
+           "kv_append", "kv_conv_append", "prefill", "prefill_inputs"]

@@ -22,6 +22,7 @@ EXPORTED = (
     "inkling_rel_attn_decode_multi_workspace_size",
     "inkling_rel_attn_prefill",
     "inkling_rel_attn_kv_append",
+    "inkling_rel_attn_kv_conv_append",
     "inkling_rel_attn_choose_splits",
     "inkling_rel_attn_decode_workspace_size",
     "inkling_rel_attn_prefill_workspace_size",
@@ -62,6 +63,11 @@ _SIGS = {
     "inkling_rel_attn_kv_append": (ctypes.c_int, [
         _p, _p, _p, _p, _p, _i32,                   # k_new v_new cu seq_lens page_table stride
         _i32, _i32, _i32, _i32, _i32, _i32,         # B T H_kv D page_size num_pages
+        _p, _p, _p, _p]),                           # k_cache v_cache err stream
+    "inkling_rel_attn_kv_conv_append": (ctypes.c_int, [
+        _p, _p, _p, _p, _p, _i32,                   # k_new v_new cu seq_lens page_table stride
+        _p, _p, _i32, _p, _p, _p, _i32,             # w_k w_v width state_k state_v slots num_slots
+        _i32, _i32, _i32, _i32, _i32, _i32, _i32,   # B T max_q_len H_kv D page_size num_pages
         _p, _p, _p, _p]),                           # k_cache v_cache err stream
     "inkling_rel_attn_choose_splits": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "inkling_rel_attn_decode_workspace_size": (_sz, [_i32] * 8),
@@ -151,6 +157,18 @@ def inkling_rel_attn_kv_append(k_new, v_new, cu_seqlens_q, seq_lens, page_table,
         _v(k_new), _v(v_new), _v(cu_seqlens_q), _v(seq_lens), _v(page_table), page_table_stride,
         B, T, H_kv, D, page_size, num_pages, _v(k_cache), _v(v_cache), _v(device_error),
         _v(stream))
+
+
+def inkling_rel_attn_kv_conv_append(k_new, v_new, cu_seqlens_q, seq_lens, page_table,
+                                    page_table_stride, conv_w_k, conv_w_v, width, conv_state_k,
+                                    conv_state_v, state_slots, num_slots, B, T, max_q_len, H_kv,
+                                    D, page_size, num_pages, k_cache, v_cache, device_error,
+                                    stream):
+    return load().inkling_rel_attn_kv_conv_append(
+        _v(k_new), _v(v_new), _v(cu_seqlens_q), _v(seq_lens), _v(page_table), page_table_stride,
+        _v(conv_w_k), _v(conv_w_v), width, _v(conv_state_k), _v(conv_state_v), _v(state_slots),
+        num_slots, B, T, max_q_len, H_kv, D, page_size, num_pages, _v(k_cache), _v(v_cache),
+        _v(device_error), _v(stream))
 
 
 def inkling_rel_attn_choose_splits(B, H_kv, window, max_seq_len, num_sms):

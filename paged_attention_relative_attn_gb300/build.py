@@ -18,7 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libinkling_rel_attn.so")
-SOURCES = ["api.cu", "decode.cu", "decode_noalloc.cu", "prefill.cu", "selftest.cu", "kv_append.cu"]
+SOURCES = ["api.cu", "decode.cu", "decode_noalloc.cu", "prefill.cu", "selftest.cu", "kv_append.cu",
+           "kv_conv.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "tc.cuh", "plan.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

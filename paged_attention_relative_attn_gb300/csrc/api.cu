@@ -392,4 +392,60 @@ int inkling_rel_attn_kv_append(const void* k_new, const void* v_new, const int32
   return launch_kv_append(c);
 }
 
+int inkling_rel_attn_kv_conv_append(const void* k_new, const void* v_new,
+                                    const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                                    const int32_t* page_table, int32_t page_table_stride,
+                                    const float* conv_w_k, const float* conv_w_v, int32_t width,
+                                    void* conv_state_k, void* conv_state_v,
+                                    const int32_t* state_slots, int32_t num_slots, int32_t B,
+                                    int32_t T, int32_t max_q_len, int32_t H_kv, int32_t D,
+                                    int32_t page_size, int32_t num_pages, void* k_cache,
+                                    void* v_cache, int32_t* device_error, void* stream) {
+  if (B < 0 || T < 0 || H_kv <= 0 || (D != 64 && D != 128)) return INKLING_ERR_ARG;
+  if (width < 1 || width > 8 || max_q_len < 0) return INKLING_ERR_ARG;
+  if (page_size <= 0 || page_size % 16 != 0 || page_size > 256) return INKLING_ERR_ARG;
+  if (num_pages <= 0 || page_table_stride <= 0) return INKLING_ERR_ARG;
+  if ((int64_t)page_table_stride * page_size > INT32_MAX) return INKLING_ERR_ARG;
+  if (width > 1 && num_slots <= 0) return INKLING_ERR_ARG;
+  if (B == 0 || T == 0 || max_q_len == 0) return INKLING_OK;
+  if (!k_new || !v_new || !cu_seqlens_q || !seq_lens || !page_table || !k_cache || !v_cache ||
+      !conv_w_k || !conv_w_v)
+    return INKLING_ERR_ARG;
+  if (width > 1 && (!conv_state_k || !conv_state_v || !state_slots)) return INKLING_ERR_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(conv_state_k, 16) || !aligned(conv_state_v, 16) ||
+      !aligned(conv_w_k, 4) || !aligned(conv_w_v, 4) || !aligned(state_slots, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(seq_lens, 4) || !aligned(page_table, 4) ||
+      !aligned(device_error, 4))
+    return INKLING_ERR_ALIGN;
+  const DevInfo di = device_info();
+  if (di.ok != 1) return INKLING_ERR_DEVICE;
+  KvConvCall c;
+  c.k_new = k_new;
+  c.v_new = v_new;
+  c.w_k = conv_w_k;
+  c.w_v = conv_w_v;
+  c.state_k = conv_state_k;
+  c.state_v = conv_state_v;
+  c.state_slots = state_slots;
+  c.cu_seqlens_q = cu_seqlens_q;
+  c.seq_lens = seq_lens;
+  c.page_table = page_table;
+  c.pt_stride = page_table_stride;
+  c.width = width;
+  c.num_slots = width > 1 ? num_slots : 0;
+  c.B = B;
+  c.T = T;
+  c.max_q_len = max_q_len;
+  c.H_kv = H_kv;
+  c.D = D;
+  c.P = page_size;
+  c.num_pages = num_pages;
+  c.k_cache = k_cache;
+  c.v_cache = v_cache;
+  c.dev_err = device_error;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return launch_kv_conv_append(c);
+}
+
 }  // extern "C"

@@ -66,9 +66,29 @@ struct KvAppendCall {
   cudaStream_t stream;
 };
 
+struct KvConvCall {
+  const void* k_new;
+  const void* v_new;
+  const float* w_k;
+  const float* w_v;
+  void* state_k;
+  void* state_v;
+  const int32_t* state_slots;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  int32_t pt_stride;
+  int32_t width, num_slots, B, T, max_q_len, H_kv, D, P, num_pages;
+  void* k_cache;
+  void* v_cache;
+  int32_t* dev_err;
+  cudaStream_t stream;
+};
+
 int launch_decode(const DecodeCall& c);        // returns INKLING_* code
 int launch_prefill(const PrefillCall& c);      // returns INKLING_* code
 int launch_kv_append(const KvAppendCall& c);   // returns INKLING_* code
+int launch_kv_conv_append(const KvConvCall& c);  // returns INKLING_* code
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,

@@ -1,0 +1,233 @@
+// Causal short convolution on K and V, fused ahead of the KV append.
+//
+// Operation: inkling_rel_attn_kv_conv_append in include/inkling_rel_attn.h
+// (TensorRT-LLM PR #17062, "Architecture": two causal short convolutions
+// inside attention, on K and on V, carrying per-request state across decode
+// steps; "pyexecutor" row: a state pool with one row per request).
+//
+// y_t[c] = sum_j w[c, j] * x_{t-(w-1)+j}[c], depthwise over the H_kv * D
+// channels of a token's row; the inputs before a request's new tokens come
+// from its state row (its last w-1 inputs, oldest first), which is replaced
+// by the last w-1 inputs of this call.  The convolved rows are written into
+// the paged cache at the tokens' positions (as inkling_rel_attn_kv_append).
+//
+// Grid: x = channel blocks of 4 * 128 channels, y = (sequence, segment of 32
+// new tokens), z = K or V: small CTAs, many of them, so that the last wave is
+// short.  A thread owns 4 adjacent channels (8-byte loads and stores, 256
+// contiguous bytes per warp and token), keeps the last w-1 inputs in registers
+// and walks its segment's tokens in order, loading eight tokens ahead; the
+// cache slot advances with the position (one page-table read per page
+// crossed, no division per token).  Only the first segment of a sequence reads the old state
+// (later segments start w-1 tokens back inside the new tokens, since a segment
+// is longer than any window), and the same thread that read a channel's old
+// state writes its new one -- so the pool row is updated in place without a
+// race between CTAs.  fp32 accumulation with the taps in order j = 0 .. w-1.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "plan.cuh"
+
+namespace ira {
+
+constexpr int kConvThreads = 128;
+constexpr int kConvSeg = 32;     // new tokens per CTA (>= the widest window)
+constexpr int kConvAhead = 8;    // tokens loaded ahead per thread
+constexpr int kConvChan = 4;     // channels per thread
+
+struct KvConvParams {
+  const uint2* x[2];       // k_new, v_new: [T][C / 4] of 4 x bf16
+  const float* w[2];       // [C][width]
+  uint2* state[2];         // [num_slots][width - 1][C / 4]
+  uint2* cache[2];         // [num_pages][P][C / 4]
+  const int32_t* cu;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  const int32_t* slots;
+  int32_t* dev_err;
+  int B, T, pt_stride, P, num_pages, num_slots, C4, segs;
+};
+
+__device__ __forceinline__ float4 bf4_to_f4(uint2 u) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ uint2 f4_to_bf4(float4 f) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(f.x, f.y);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.z, f.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  return u;
+}
+
+template <int W>
+__global__ void __launch_bounds__(kConvThreads)
+    kv_conv_append_kernel(const __grid_constant__ KvConvParams p) {
+  constexpr int NS = W - 1;  // state rows
+  const int which = blockIdx.z;
+  const int b = blockIdx.y / p.segs;
+  const int seg = blockIdx.y - b * p.segs;
+  const int c4 = blockIdx.x * kConvThreads + threadIdx.x;
+  const bool reporter = threadIdx.x == 0 && blockIdx.x == 0 && which == 0;
+
+  const int t0 = __ldg(p.cu + b);
+  const int q_len = __ldg(p.cu + b + 1) - t0;
+  const int s0 = seg * kConvSeg;
+  if (q_len <= 0 || s0 >= q_len) return;
+  const int L = __ldg(p.seq_lens + b);
+  const int slot = NS > 0 ? __ldg(p.slots + b) : 0;
+  if (q_len > L || t0 < 0 || t0 + q_len > p.T) {
+    if (reporter && seg == 0) report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);
+    return;
+  }
+  if (NS > 0 && (slot < 0 || slot >= p.num_slots)) {
+    if (reporter && seg == 0) report(p.dev_err, INKLING_DEVERR_BAD_SLOT);
+    return;
+  }
+  if (seg == p.segs - 1 && s0 + kConvSeg < q_len && reporter)
+    report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);  // tokens past max_q_len are not written
+  if (c4 >= p.C4) return;
+
+  const uint2* __restrict__ x = p.x[which] + (size_t)t0 * p.C4 + c4;
+  uint2* __restrict__ st = p.state[which] + (size_t)slot * NS * p.C4 + c4;
+  uint2* __restrict__ cache = p.cache[which] + c4;
+  const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride;
+
+  // taps of this thread's 4 channels: 4 * W contiguous floats, read as W
+  // 16-byte vectors when the tap array is 16-byte aligned
+  float wt[kConvChan][W];
+  {
+    const float* wp = p.w[which] + (size_t)c4 * kConvChan * W;
+    if ((reinterpret_cast<uintptr_t>(p.w[which]) & 15) == 0) {
+#pragma unroll
+      for (int v = 0; v < W; ++v) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(wp) + v);
+        wt[(4 * v) / W][(4 * v) % W] = f.x;
+        wt[(4 * v + 1) / W][(4 * v + 1) % W] = f.y;
+        wt[(4 * v + 2) / W][(4 * v + 2) % W] = f.z;
+        wt[(4 * v + 3) / W][(4 * v + 3) % W] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < kConvChan; ++c)
+#pragma unroll
+        for (int j = 0; j < W; ++j) wt[c][j] = __ldg(wp + c * W + j);
+    }
+  }
+
+  // the w-1 inputs before the segment: chunk-relative r = s0 - NS + j
+  uint2 win[NS > 0 ? NS : 1];
+#pragma unroll
+  for (int j = 0; j < NS; ++j) {
+    if (seg == 0) win[j] = st[(size_t)j * p.C4];  // r = j - NS < 0: state row j
+    else win[j] = __ldcs(x + (size_t)(s0 - NS + j) * p.C4);
+  }
+
+  const int s1 = min(s0 + kConvSeg, q_len);
+  int lp = (L - q_len + s0) / p.P;             // logical page of the segment's first token
+  int in_page = (L - q_len + s0) - lp * p.P;   // its slot
+  size_t row0 = 0;                             // first row of the current physical page
+  bool page_ok = false;
+  auto enter_page = [&]() {  // checks once per page crossed
+    if (lp >= p.pt_stride) {
+      page_ok = false;
+      if (threadIdx.x == 0) report(p.dev_err, INKLING_DEVERR_SEQ_TOO_LONG);
+      return;
+    }
+    const int page = __ldg(pt_row + lp);
+    page_ok = page >= 0 && page < p.num_pages;
+    if (!page_ok && threadIdx.x == 0) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
+    row0 = (size_t)page * p.P * p.C4;
+  };
+  enter_page();
+  for (int tb = s0; tb < s1; tb += kConvAhead) {
+    uint2 xin[kConvAhead];
+#pragma unroll
+    for (int u = 0; u < kConvAhead; ++u)
+      if (tb + u < s1) xin[u] = __ldcs(x + (size_t)(tb + u) * p.C4);
+#pragma unroll
+    for (int u = 0; u < kConvAhead; ++u) {
+      const int t = tb + u;
+      if (t >= s1) break;
+      float acc[kConvChan] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const float4 v = bf4_to_f4(j < NS ? win[j < NS ? j : 0] : xin[u]);
+        acc[0] = fmaf(wt[0][j], v.x, acc[0]);
+        acc[1] = fmaf(wt[1][j], v.y, acc[1]);
+        acc[2] = fmaf(wt[2][j], v.z, acc[2]);
+        acc[3] = fmaf(wt[3][j], v.w, acc[3]);
+      }
+#pragma unroll
+      for (int j = 0; j + 1 < NS; ++j) win[j] = win[j + 1];
+      if (NS > 0) win[NS > 0 ? NS - 1 : 0] = xin[u];
+      if (page_ok)
+        cache[row0 + (size_t)in_page * p.C4] = f4_to_bf4(make_float4(acc[0], acc[1], acc[2], acc[3]));
+      if (++in_page == p.P && t + 1 < s1) {  // the next token starts the next logical page
+        in_page = 0;
+        ++lp;
+        enter_page();
+      }
+    }
+  }
+
+  // new state: the last w-1 inputs of the sequence.  When all its new tokens
+  // fall in this first segment, the window now holds exactly those (it began
+  // as the old state and took every new token); otherwise they are the last
+  // w-1 new tokens (q_len > kConvSeg >= w-1).
+  if (seg == 0) {
+    if (q_len <= kConvSeg) {
+#pragma unroll
+      for (int j = 0; j < NS; ++j) st[(size_t)j * p.C4] = win[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < NS; ++j) st[(size_t)j * p.C4] = __ldcs(x + (size_t)(q_len - NS + j) * p.C4);
+    }
+  }
+}
+
+int launch_kv_conv_append(const KvConvCall& c) {
+  KvConvParams prm;
+  prm.x[0] = static_cast<const uint2*>(c.k_new);
+  prm.x[1] = static_cast<const uint2*>(c.v_new);
+  prm.w[0] = c.w_k;
+  prm.w[1] = c.w_v;
+  prm.state[0] = static_cast<uint2*>(c.state_k);
+  prm.state[1] = static_cast<uint2*>(c.state_v);
+  prm.cache[0] = static_cast<uint2*>(c.k_cache);
+  prm.cache[1] = static_cast<uint2*>(c.v_cache);
+  prm.cu = c.cu_seqlens_q;
+  prm.seq_lens = c.seq_lens;
+  prm.page_table = c.page_table;
+  prm.slots = c.state_slots;
+  prm.dev_err = c.dev_err;
+  prm.B = c.B;
+  prm.T = c.T;
+  prm.pt_stride = c.pt_stride;
+  prm.P = c.P;
+  prm.num_pages = c.num_pages;
+  prm.num_slots = c.num_slots;
+  prm.C4 = c.H_kv * c.D / kConvChan;
+  prm.segs = (c.max_q_len + kConvSeg - 1) / kConvSeg;
+  const int64_t gy = (int64_t)c.B * prm.segs;  // (sequence, segment) pairs
+  if (gy <= 0 || gy > 65535) return INKLING_ERR_ARG;
+  const dim3 grid((prm.C4 + kConvThreads - 1) / kConvThreads, (unsigned)gy, 2);
+  switch (c.width) {
+    case 1: kv_conv_append_kernel<1><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    case 2: kv_conv_append_kernel<2><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    case 3: kv_conv_append_kernel<3><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    case 4: kv_conv_append_kernel<4><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    case 5: kv_conv_append_kernel<5><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    case 6: kv_conv_append_kernel<6><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    case 7: kv_conv_append_kernel<7><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    case 8: kv_conv_append_kernel<8><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
+    default: return INKLING_ERR_ARG;
+  }
+  return cudaGetLastError() == cudaSuccess ? INKLING_OK : INKLING_ERR_CUDA;
+}
+
+}  // namespace ira

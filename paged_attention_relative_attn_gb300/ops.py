@@ -202,6 +202,52 @@ def kv_append(k_new, v_new, cu_seqlens_q, seq_lens, page_table, k_cache, v_cache
     _check(rc, "inkling_rel_attn_kv_append")
 
 
+def kv_conv_append(k_new, v_new, cu_seqlens_q, seq_lens, page_table, k_cache, v_cache,
+                   conv_w_k, conv_w_v, conv_state_k, conv_state_v, state_slots, *,
+                   max_q_len, device_error=None, stream=None):
+    """The causal short convolutions on K and V of the new tokens, then the
+    append of the convolved rows into the paged cache; the state pool rows of
+    the sequences are rewritten in place.  See inkling_rel_attn_kv_conv_append.
+
+    k_new, v_new [T, H_kv, D] bf16; conv_w_k, conv_w_v [H_kv, D, width] fp32;
+    conv_state_k, conv_state_v [num_slots, width - 1, H_kv, D] bf16 (width 1:
+    None); state_slots [B] int32; the rest as for ``kv_append``.  max_q_len is
+    a host bound on any sequence's new tokens.
+    """
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(conv_w_k, "conv_w_k", torch.float32, 3)
+    _need(conv_w_v, "conv_w_v", torch.float32, 3)
+    T, H_kv, D = k_new.shape
+    num_pages, P, H_kv_c, D_c = k_cache.shape
+    B = seq_lens.shape[0]
+    width = conv_w_k.shape[2]
+    if (v_new.shape != k_new.shape or v_cache.shape != k_cache.shape or (H_kv_c, D_c) != (H_kv, D)
+            or cu_seqlens_q.shape[0] != B + 1 or page_table.shape[0] != B
+            or tuple(conv_w_k.shape) != (H_kv, D, width) or conv_w_v.shape != conv_w_k.shape):
+        raise ValueError("inconsistent shapes")
+    num_slots = 0
+    if width > 1:
+        _need(conv_state_k, "conv_state_k", torch.bfloat16, 4)
+        _need(conv_state_v, "conv_state_v", torch.bfloat16, 4)
+        _need(state_slots, "state_slots", torch.int32, 1)
+        num_slots = conv_state_k.shape[0]
+        if (tuple(conv_state_k.shape) != (num_slots, width - 1, H_kv, D)
+                or conv_state_v.shape != conv_state_k.shape or state_slots.shape[0] != B):
+            raise ValueError("inconsistent state shapes")
+    rc = _lib.inkling_rel_attn_kv_conv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(page_table),
+        page_table.shape[1], _ptr(conv_w_k), _ptr(conv_w_v), width, _ptr(conv_state_k),
+        _ptr(conv_state_v), _ptr(state_slots), num_slots, B, T, int(max_q_len), H_kv, D, P,
+        num_pages, _ptr(k_cache), _ptr(v_cache), _ptr(device_error), _stream(k_new.device, stream))
+    _check(rc, "inkling_rel_attn_kv_conv_append")
+
+
 def decode_inputs(inp, **kw):
     """``decode`` on a workloads.DecodeInputs-like object."""
     return decode(inp.q, inp.k_cache, inp.v_cache, inp.page_table, inp.seq_lens, inp.rel_logits,

@@ -134,6 +134,29 @@ def test_kv_append_argument_validation(lib):
     assert rc(seq_lens=6) == -2
 
 
+def test_kv_conv_append_argument_validation(lib):
+    a = dict(k_new=16, v_new=16, cu_seqlens_q=4, seq_lens=4, page_table=4, page_table_stride=4,
+             conv_w_k=4, conv_w_v=4, width=4, conv_state_k=16, conv_state_v=16, state_slots=4,
+             num_slots=3, B=2, T=2, max_q_len=2, H_kv=2, D=64, page_size=16, num_pages=8,
+             k_cache=16, v_cache=16, device_error=None, stream=None)
+    rc = lambda **o: lib.inkling_rel_attn_kv_conv_append(**{**a, **o})  # noqa: E731
+    assert rc(width=0) == -1
+    assert rc(width=9) == -1
+    assert rc(D=96) == -1
+    assert rc(page_size=24) == -1
+    assert rc(num_slots=0) == -1        # a state pool is needed when width > 1
+    assert rc(max_q_len=-1) == -1
+    assert rc(B=0) == 0 and rc(T=0) == 0 and rc(max_q_len=0) == 0
+    assert rc(conv_w_k=None) == -1
+    assert rc(conv_state_v=None) == -1
+    assert rc(conv_state_k=24) == -2    # 16-byte alignment
+    assert rc(conv_w_v=2) == -2
+    # width 1 needs no state: with the state pointers NULL the call gets as far
+    # as the alignment check (it would stop at -1 if they were required)
+    assert rc(width=1, num_slots=0, conv_state_k=None, conv_state_v=None, state_slots=None,
+              k_cache=24) == -2
+
+
 def test_decode_multi_validation_and_workspace(lib):
     a = dict(q=16, k_cache=16, v_cache=16, page_table=4, page_table_stride=4, seq_lens=4,
              rel_logits=4, B=2, q_len=4, H_q=4, H_kv=2, D=64, page_size=16, num_pages=16, R=32,
