@@ -284,7 +284,8 @@ int inkling_rel_attn_kv_append(
  * 65535).  On the device: an
  * inconsistent chunk (q_len_b > seq_lens[b]) sets INKLING_DEVERR_BAD_CHUNK and
  * the sequence is skipped; q_len_b > max_q_len sets it too and the tokens past
- * max_q_len are not written; a state row outside [0, num_slots) sets
+ * max_q_len are not written (the state row still moves to the end of the
+ * chunk); a state row outside [0, num_slots) sets
  * INKLING_DEVERR_BAD_SLOT and the sequence is skipped; positions past the
  * page-table row and bad page ids set INKLING_DEVERR_SEQ_TOO_LONG /
  * INKLING_DEVERR_BAD_PAGE and those rows are not written.
