@@ -44,6 +44,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "rel-bias paged attn: decode KV GB/s (% of HBM peak); prefill TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
+BUSY_WINDOW_S = 0.15  # untimed load before and after the timed region (clock samples)
 
 
 # ---------------------------------------------------------------------------
@@ -95,6 +96,13 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_first(self, timeout_s=5.0):
+        """Block until nvidia-smi has printed its first sample (it takes a
+        moment to start), so that samples cover what runs next."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.01)
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -220,9 +228,21 @@ def time_steps(args, device, step, K, warmup, per_graph):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(args)
-    torch.cuda.synchronize()
+
+    def keep_busy(seconds):
+        # untimed replays of the same graph, so that the clock samples taken
+        # around a short timed region still see the GPU under this load
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            with torch.cuda.stream(cap):
+                g_main.replay()
+            torch.cuda.synchronize()
+
     with ClockSampler(torch.cuda.current_device()) as clk:
+        clk.wait_first()
+        keep_busy(BUSY_WINDOW_S)
+        barrier(args)
+        torch.cuda.synchronize()
         with torch.cuda.stream(cap):
             ev0.record(cap)
             for _ in range(reps):
@@ -231,33 +251,57 @@ def time_steps(args, device, step, K, warmup, per_graph):
                 g_rem.replay()
             ev1.record(cap)
         torch.cuda.synchronize()
-    barrier(args)
+        barrier(args)
+        keep_busy(BUSY_WINDOW_S)
     ms = max_over_ranks(args, ev0.elapsed_time(ev1))
-    return ms, clk.summary()
+    summary = clk.summary()
+    summary["window"] = (f"nvidia-smi every 50 ms over the timed region plus {BUSY_WINDOW_S:.2f} s "
+                         f"of untimed replays of the same steps before and after it")
+    return ms, summary
 
 
-def decode_workload_config(name, batch=None):
-    """The static description of a decode workload (the same in both arms)."""
+def decode_rotation(name, batch=None, n_sets=None):
+    """Visible K+V bytes of each input set the decode bench rotates through:
+    sets are added (seed = set index) until one rotation's visible K/V exceeds
+    2 x L2, at least 3, or exactly ``n_sets``.  Only the drawn lengths matter,
+    so both arms compute it without building the inputs."""
     c = W.DECODE_CONFIGS[name]
-    B = c["B"] if batch is None else batch
+    lo, hi = c["len_range"]
+    per = []
+    while True:
+        lens = W.draw_uniform_lengths(c["B"], lo, hi, len(per))
+        if batch is not None:
+            lens = lens[:batch]
+        vis = [min(L, c["window"]) if c["window"] > 0 else L for L in lens]
+        per.append(sum(vis) * c["H_kv"] * c["D"] * 2 * 2)
+        if n_sets is not None:
+            if len(per) >= n_sets:
+                break
+        elif len(per) >= 3 and sum(per) > 2 * L2_BYTES:
+            break
+    return per
+
+
+def decode_workload_config(args, name):
+    """The description of a decode workload, identical in both arms."""
+    c = W.DECODE_CONFIGS[name]
+    B = c["B"] if args.batch is None else args.batch
     lens = c.get("len_range")
+    per = decode_rotation(name, args.batch, args.sets)
     return {"workload": name, "batch": B, "heads": f"{c['H_q']}/{c['H_kv']}", "head_dim": c["D"],
             "page_size": c["P"], "window": c["window"], "R": c["R"],
-            "lengths": f"uniform [{lens[0]}, {lens[1]}]" if lens else "fixed"}
+            "lengths": f"uniform [{lens[0]}, {lens[1]}]" if lens else "fixed",
+            "l2": f"rotating {len(per)} input sets, {sum(per) / 1e6:.0f} MB of visible K/V per "
+                  f"rotation (L2 129 MB)",
+            "parallelism": f"replicas x{args.world}"}
 
 
 def bench_decode(args, device, name, K, warmup):
     import paged_attention_relative_attn_gb300 as ira
-    sets = []
-    while True:
-        sets.append(W.make_decode_config(name, device=device, seed=len(sets), batch=args.batch))
-        if args.sets is not None:
-            if len(sets) >= args.sets:
-                break
-        # rotate until the distinct visible K/V of one rotation exceeds 2x L2
-        elif len(sets) >= 3 and sum(decode_bytes(x)[0] for x in sets) > 2 * L2_BYTES:
-            break
-    n_sets = len(sets)
+    # rotate until the distinct visible K/V of one rotation exceeds 2x L2
+    n_sets = len(decode_rotation(name, args.batch, args.sets))
+    sets = [W.make_decode_config(name, device=device, seed=i, batch=args.batch)
+            for i in range(n_sets)]
     per_set = [decode_bytes(x) for x in sets]
     B, H_q, H_kv, D = sets[0].B, sets[0].H_q, sets[0].H_kv, sets[0].D
     S = ira.choose_splits(B, H_kv, sets[0].window, sets[0].max_seq_len,
@@ -276,13 +320,11 @@ def bench_decode(args, device, name, K, warmup):
     kv_total = sum(per_set[i % n_sets][0] for i in range(K))
     all_total = sum(per_set[i % n_sets][1] for i in range(K))
     launches = K * (1 + (1 if S > 1 else 0))
-    x0 = sets[0]
-    config = dict(decode_workload_config(name, args.batch), num_splits=S,
-                  l2=f"rotating {n_sets} input sets, {sum(p[0] for p in per_set) / 1e6:.0f} MB of "
-                     f"visible K/V per rotation (L2 129 MB)")
+    config = decode_workload_config(args, name)
+    assert config["l2"].startswith(f"rotating {n_sets} ")
     return dict(ms=ms, K=K, clocks=clocks, launches=launches, config=config, sets=sets, ws=ws,
                 units_total=kv_total, bytes_total=all_total, kernel="decode_kernel",
-                kernel_launches=K, unit="GB/s")
+                kernel_launches=K, unit="GB/s", launch={"num_splits": S})
 
 
 def prefill_work(inp, window):
@@ -681,8 +723,9 @@ def bench_decode_e2e(args, device, sets, ws, nbuf=2):
 def oracle_units(inp, budget_s, max_units=None):
     """Time the oracle, as it stands, on (sequence, KV-head group) units of a
     decode batch until ~budget_s of CPU work (at least one unit).  Only the
-    pages a unit uses are copied to the host.  Returns (GB/s of visible K+V,
-    units done, seconds)."""
+    pages a unit uses are gathered into fp64 host arrays; that preparation is
+    timed with the oracle call.  Returns (GB/s of visible K+V, units done,
+    seconds)."""
     from oracle.ref import ref_decode
     P = inp.page_size
     G = inp.H_q // inp.H_kv
@@ -691,6 +734,7 @@ def oracle_units(inp, budget_s, max_units=None):
     n = 0
     total = inp.B * inp.H_kv
     for u in range(total):
+        t0 = time.perf_counter()
         b, hk = divmod(u, inp.H_kv)
         L = int(inp.seq_lens[b])
         npg = (L + P - 1) // P
@@ -700,7 +744,6 @@ def oracle_units(inp, budget_s, max_units=None):
         pt = np.arange(npg, dtype=np.int64)[None, :]
         q = inp.q[b:b + 1, hk * G:(hk + 1) * G].float().cpu().numpy().astype(np.float64)
         rel = inp.rel_logits[b:b + 1, hk * G:(hk + 1) * G].float().cpu().numpy().astype(np.float64)
-        t0 = time.perf_counter()
         ref_decode(q, kc, vc, pt, np.array([L]), rel, inp.window, inp.scale)
         t_used += time.perf_counter() - t0
         vis = min(L, inp.window) if inp.window > 0 else L
@@ -709,6 +752,11 @@ def oracle_units(inp, budget_s, max_units=None):
         if t_used >= budget_s or (max_units and n >= max_units):
             break
     return done_bytes / t_used / 1e9, n, t_used
+
+
+def cpu_cores():
+    """(host cores, BLAS threads the oracle's NumPy uses)."""
+    return os.cpu_count() or 1, blas_threads()
 
 
 def blas_threads():
@@ -753,30 +801,38 @@ def sum_over_ranks(args, x):
 
 def run_reference(args):
     """The oracle arm: rank 0 only, on host cores.  Each step is a bounded
-    sample of (sequence, KV-head) units of the workload, sized so the whole
-    run stays within a few minutes."""
+    sample of (sequence, KV-head) units of the workload -- every unit of its
+    first 4 sequences, or as many as fit the per-step budget -- sized so the
+    whole run stays within a few minutes.  ms_per_step is the measured time
+    of a step."""
     if args.rank != 0:
         return
     n_seq = 4
     inp = W.make_decode_config(args.workload, device="cpu", seed=0, batch=n_seq)
     per_step = min(args.ref_budget, max(0.002, 150.0 / max(1, args.steps + args.warmup)))
-    vals = []
+    vals, secs = [], []
     units = 0
     for i in range(args.warmup + args.steps):
-        gbs, n, _ = oracle_units(inp, per_step)
+        gbs, n, t = oracle_units(inp, per_step)
         if i >= args.warmup:
             vals.append(gbs)
+            secs.append(t)
             units += n
     v = statistics.median(vals)
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+    cores, blas = cpu_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.median(secs) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": decode_workload_config(args.workload, getattr(args, "batch", None)),
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+            "config": decode_workload_config(args, args.workload),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "blas_threads": blas,
+                             "kind": "oracle",
                              "sample": f"per step: (sequence, KV head) units of the first "
-                                       f"{n_seq} sequences of {args.workload}, ~{per_step:.3f} s "
-                                       f"of fp64 oracle time; {units} units timed"},
+                                       f"{n_seq} sequences of {args.workload} (all "
+                                       f"{n_seq * inp.H_kv}, or as many as fit "
+                                       f"{per_step:.3f} s); {units} units timed over "
+                                       f"{args.steps} steps, {sum(secs):.2f} s"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -823,24 +879,28 @@ def summarize(args, r, pk):
     bytes_per_launch = r["bytes_total"] / r["kernel_launches"]
     achieved = bytes_per_launch / per_launch_s / 1e9
     name = r["config"]["workload"]
+    r["config"].setdefault("parallelism", f"replicas x{args.world}")
     roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / pk["hbm_gbs"],
             "traffic": traffic_record(r["kernel"], name, KERNEL_SOURCES[r["kernel"]]),
             "kernel": r["kernel"], "peak_source": f"{pk['source']} hbm_gbs (of {pk['source']})",
             "bytes_per_launch": bytes_per_launch}
     out = {"value": None, "unit": r["unit"], "ms_per_step": ms / r["K"], "steps": r["K"],
-           "config": r["config"], "clocks": r["clocks"], "gpu_launches": r["launches"]}
+           "config": r["config"], "clocks": r["clocks"], "gpu_launches": r["launches"],
+           "launch": dict(r.get("launch", {}),
+                          timing="CUDA graph replay of exactly K steps, CUDA events")}
     if r["unit"] == "TFLOP/s":
         tflops = units / sec / 1e12
         out["value"] = tflops
         out["metric"] = METRIC + " [prefill TFLOP/s]"
         if r.get("bound") == "tensor":
-            # a seconds-long loop of one kernel: the sustained bf16 figure applies
-            peak = pk["bf16_tflops_sustained"]
+            # one kernel timed alone for a fraction of a second: the burst
+            # bf16 figure applies
+            peak = pk["bf16_tflops"]
             roof = {"bound": "tensor", "achieved": tflops / args.world, "peak": peak,
                     "unit": "TFLOP/s", "frac": tflops / args.world / peak,
                     "traffic": roof["traffic"], "kernel": r["kernel"],
-                    "peak_source": f"{pk['source']} bf16_tflops_sustained (of {pk['source']})",
+                    "peak_source": f"{pk['source']} bf16_tflops, burst (of {pk['source']})",
                     "flops_per_launch": r["units_total"] / r["kernel_launches"],
                     "hbm_achieved_gbs": achieved, "hbm_frac": achieved / pk["hbm_gbs"]}
         else:
@@ -901,8 +961,7 @@ def main():
             "n_gpus": args.world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(head["config"], parallelism=f"replicas x{args.world}",
-                           timing="CUDA graph replay of exactly K steps, CUDA events"),
+            "config": head["config"], "launch": head["launch"],
             "clocks": head["clocks"], "gpu_launches": head["gpu_launches"],
             "roofline": head["roofline"]}
     if args.workload in ("local_decode", "global_decode") and not args.no_e2e:
@@ -913,8 +972,9 @@ def main():
         line["e2e"] = None
     if args.rank == 0 and not args.no_cpu_baseline and "sets" in r:
         gbs, n, t = oracle_units(r["sets"][0], args.cpu_budget)
-        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": blas_threads(),
-                                "kind": "oracle",
+        cores, blas = cpu_cores()
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores,
+                                "blas_threads": blas, "kind": "oracle",
                                 "sample": f"{n} (sequence, KV head) units of {args.workload} "
                                           f"(first of {r['sets'][0].B * r['sets'][0].H_kv}), "
                                           f"{t:.1f} s of fp64 oracle time"}

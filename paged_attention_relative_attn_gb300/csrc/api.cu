@@ -85,6 +85,16 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, vo
   return r == CUDA_SUCCESS;
 }
 
+bool smem_limit_on_device(const void* kern, int bytes, std::atomic<int>* done) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+  if (dev < kMaxDevices && done[dev].load(std::memory_order_acquire) == bytes) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  if (dev < kMaxDevices) done[dev].store(bytes, std::memory_order_release);
+  return true;
+}
+
 // ---------------------------------------------------------------- device info
 struct DevInfo {
   int ok;  // 1 = sm_103, 0 = other, -1 = query failed
@@ -92,11 +102,11 @@ struct DevInfo {
 };
 
 static DevInfo device_info() {
-  static std::atomic<int> cached_ok[64];
-  static std::atomic<int> cached_sms[64];
+  static std::atomic<int> cached_ok[kMaxDevices];
+  static std::atomic<int> cached_sms[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return {-1, 0};
-  if (dev < 64) {
+  if (dev < kMaxDevices) {
     int ok = cached_ok[dev].load(std::memory_order_relaxed);
     if (ok != 0) return {ok > 0 ? 1 : 0, cached_sms[dev].load(std::memory_order_relaxed)};
   }
@@ -106,7 +116,7 @@ static DevInfo device_info() {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return {-1, 0};
   const int ok = (major == 10 && minor == 3) ? 1 : 0;
-  if (dev < 64) {
+  if (dev < kMaxDevices) {
     cached_sms[dev].store(sms, std::memory_order_relaxed);
     cached_ok[dev].store(ok ? 1 : -1, std::memory_order_relaxed);
   }

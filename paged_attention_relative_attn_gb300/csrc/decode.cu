@@ -40,7 +40,6 @@
 
 #include <algorithm>
 #include <cstring>
-#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -1030,12 +1029,9 @@ static int sm_count() {
 template <int D, int NT, int BH, bool MULTI, bool COMB2 = false>
 static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int smem_bytes, int grid) {
   auto kern = decode_kernel<D, NT, BH, MULTI, COMB2>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  });
-  if (attr_err != cudaSuccess) return INKLING_ERR_CUDA;
+  static std::atomic<int> limit_set[kMaxDevices];
+  if (!smem_limit_on_device(reinterpret_cast<const void*>(kern), 227 * 1024, limit_set))
+    return INKLING_ERR_CUDA;
   kern<<<grid, kDecodeThreads, smem_bytes, c.stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return INKLING_ERR_CUDA;
   return INKLING_OK;

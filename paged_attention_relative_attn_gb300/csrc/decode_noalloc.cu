@@ -36,13 +36,13 @@ constexpr size_t kInklingNoallocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kInklingNoallocScratchBytes];
 
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[64] = {};
+void* g_scratch_ptr[ira::kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (looked up once
 // per device), or nullptr on failure.
 void* scratch_for_current_device() {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= ira::kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_ptr[dev]) {
     void* ptr = nullptr;
@@ -63,14 +63,14 @@ extern "C" int inkling_rel_attn_decode_noalloc(
   const size_t need = inkling_rel_attn_decode_workspace_size(B, H_q, H_kv, D, window, max_seq_len,
                                                              num_splits, 0);
   if (need > kInklingNoallocScratchBytes) return INKLING_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  if (need > 0) {
-    scratch = scratch_for_current_device();
-    if (!scratch) return INKLING_ERR_CUDA;
-  }
+  // resolved on every call (cached after the first on each device), whether
+  // or not this call splits, so the first call on a device is always the one
+  // that does the look-up
+  void* scratch = scratch_for_current_device();
+  if (!scratch) return INKLING_ERR_CUDA;
   return inkling_rel_attn_decode(q, k_cache, v_cache, page_table, page_table_stride, seq_lens,
                                  rel_logits, B, H_q, H_kv, D, page_size, num_pages, R, window,
-                                 scale, max_seq_len, out, lse_out, scratch,
+                                 scale, max_seq_len, out, lse_out, need > 0 ? scratch : nullptr,
                                  need > 0 ? kInklingNoallocScratchBytes : 0, num_splits,
                                  device_error, stream);
 }

@@ -6,9 +6,21 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/inkling_rel_attn.h"
 
 namespace ira {
+
+// Devices a process may drive for which per-device state is cached.
+constexpr int kMaxDevices = 64;
+
+// Raise `kern`'s dynamic shared-memory limit to `bytes` on the current device.
+// Function attributes belong to each device's context, so this is done once
+// per (kernel, device): `done` is the kernel's own kMaxDevices-entry table
+// (zero-initialised), holding the limit already set on each device.  Returns
+// false when the device query or the attribute call fails.
+bool smem_limit_on_device(const void* kern, int bytes, std::atomic<int>* done);
 
 // Validated decode call, with the split plan resolved.
 struct DecodeCall {

@@ -40,7 +40,6 @@
 
 #include <algorithm>
 #include <cstring>
-#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -772,12 +771,9 @@ template <int D, int BH>
 static int launch_prefill_t(const PrefillCall& c, const PrefillParams& prm, dim3 grid) {
   auto kern = prefill_kernel<D, BH>;
   const int smem = 1024 + PrefillSmem<D>::TOTAL;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  });
-  if (attr_err != cudaSuccess) return INKLING_ERR_CUDA;
+  static std::atomic<int> limit_set[kMaxDevices];
+  if (!smem_limit_on_device(reinterpret_cast<const void*>(kern), smem, limit_set))
+    return INKLING_ERR_CUDA;
   kern<<<grid, kPrefThreads, smem, c.stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return INKLING_ERR_CUDA;
   return INKLING_OK;

@@ -34,16 +34,20 @@ def _worker(rank, world, port, q):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
     args = types.SimpleNamespace(world=world, rank=rank, local=rank)
+    # the description our arm prints for the same workload
+    config = bench.decode_workload_config(
+        types.SimpleNamespace(world=world, batch=None, sets=None), "local_decode")
     bench.barrier(args)
     t = bench.max_over_ranks(args, 10.0 + rank)       # slowest rank wins
     u = bench.sum_over_ranks(args, 100.0 * (rank + 1))  # units add up
     # the reference arm: rank 0 prints one line, the others print nothing
     rargs = types.SimpleNamespace(world=world, rank=rank, local=rank, workload="local_decode",
-                                  steps=1, warmup=0, ref_budget=0.01, gpus=world, batch=None)
+                                  steps=2, warmup=0, ref_budget=0.01, gpus=world, batch=None,
+                                  sets=None)
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         bench.run_reference(rargs)
-    q.put((rank, t, u, buf.getvalue().strip()))
+    q.put((rank, t, u, buf.getvalue().strip(), config))
     dist.barrier()
     dist.destroy_process_group()
 
@@ -59,7 +63,7 @@ def test_two_rank_reductions_and_reference_arm():
     for p in procs:
         p.join(timeout=120)
         assert p.exitcode == 0
-    (r0, t0, u0, out0), (r1, t1, u1, out1) = res
+    (r0, t0, u0, out0, config), (r1, t1, u1, out1, _) = res
     assert t0 == t1 == 11.0
     assert u0 == u1 == 300.0
     assert out1 == ""
@@ -67,3 +71,11 @@ def test_two_rank_reductions_and_reference_arm():
     line = json.loads(out0)
     assert line["impl"] == "reference" and line["unit"] == "GB/s"
     assert line["cpu_baseline"]["kind"] == "oracle"
+    # both arms describe the workload identically
+    assert line["config"] == config
+    assert line["n_gpus"] == 2
+    # the time per step is the time spent (the per-step budget is 0.01 s and
+    # at least one unit runs), not the budget
+    assert 0 < line["ms_per_step"] < 5000
+    assert line["cpu_baseline"]["cores"] == os.cpu_count()
+    assert line["cpu_baseline"]["blas_threads"] >= 1
