@@ -11,9 +11,9 @@
 // by the last w-1 inputs of this call.  The convolved rows are written into
 // the paged cache at the tokens' positions (as inkling_rel_attn_kv_append).
 //
-// Grid: x = channel blocks of 4 * 128 channels, y = (sequence, segment of 32
+// Grid: x = channel blocks of 8 * 128 channels, y = (sequence, segment of 64
 // new tokens), z = K or V: small CTAs, many of them, so that the last wave is
-// short.  A thread owns 4 adjacent channels (8-byte loads and stores, 256
+// short.  A thread owns 8 adjacent channels (16-byte loads and stores, 512
 // contiguous bytes per warp and token), keeps the last w-1 inputs in registers
 // and walks its segment's tokens in order, loading eight tokens ahead; the
 // cache slot advances with the position (one page-table read per page
@@ -32,36 +32,41 @@
 namespace ira {
 
 constexpr int kConvThreads = 128;
-constexpr int kConvSeg = 32;     // new tokens per CTA (>= the widest window)
+constexpr int kConvSeg = 64;     // new tokens per CTA (>= the widest window)
 constexpr int kConvAhead = 8;    // tokens loaded ahead per thread
-constexpr int kConvChan = 4;     // channels per thread
+constexpr int kConvChan = 8;     // channels per thread
 
 struct KvConvParams {
-  const uint2* x[2];       // k_new, v_new: [T][C / 4] of 4 x bf16
+  const uint4* x[2];       // k_new, v_new: [T][C / 8] of 8 x bf16
   const float* w[2];       // [C][width]
-  uint2* state[2];         // [num_slots][width - 1][C / 4]
-  uint2* cache[2];         // [num_pages][P][C / 4]
+  uint4* state[2];         // [num_slots][width - 1][C / 8]
+  uint4* cache[2];         // [num_pages][P][C / 8]
   const int32_t* cu;
   const int32_t* seq_lens;
   const int32_t* page_table;
   const int32_t* slots;
   int32_t* dev_err;
-  int B, T, pt_stride, P, num_pages, num_slots, C4, segs;
+  int B, T, pt_stride, P, num_pages, num_slots, C8, segs;
 };
 
-__device__ __forceinline__ float4 bf4_to_f4(uint2 u) {
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-  return make_float4(a.x, a.y, b.x, b.y);
+// bf16 -> fp32 is exact: the bf16 bits are the high half of the float.
+__device__ __forceinline__ void bf8_to_f8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
 }
 
-__device__ __forceinline__ uint2 f4_to_bf4(float4 f) {
-  const __nv_bfloat162 a = __floats2bfloat162_rn(f.x, f.y);
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.z, f.w);
-  uint2 u;
-  u.x = *reinterpret_cast<const uint32_t*>(&a);
-  u.y = *reinterpret_cast<const uint32_t*>(&b);
-  return u;
+__device__ __forceinline__ uint4 f8_to_bf8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&a);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 template <int W>
@@ -71,7 +76,7 @@ __global__ void __launch_bounds__(kConvThreads)
   const int which = blockIdx.z;
   const int b = blockIdx.y / p.segs;
   const int seg = blockIdx.y - b * p.segs;
-  const int c4 = blockIdx.x * kConvThreads + threadIdx.x;
+  const int c8 = blockIdx.x * kConvThreads + threadIdx.x;
   const bool reporter = threadIdx.x == 0 && blockIdx.x == 0 && which == 0;
 
   const int t0 = __ldg(p.cu + b);
@@ -90,21 +95,21 @@ __global__ void __launch_bounds__(kConvThreads)
   }
   if (seg == p.segs - 1 && s0 + kConvSeg < q_len && reporter)
     report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);  // tokens past max_q_len are not written
-  if (c4 >= p.C4) return;
+  if (c8 >= p.C8) return;
 
-  const uint2* __restrict__ x = p.x[which] + (size_t)t0 * p.C4 + c4;
-  uint2* __restrict__ st = p.state[which] + (size_t)slot * NS * p.C4 + c4;
-  uint2* __restrict__ cache = p.cache[which] + c4;
+  const uint4* __restrict__ x = p.x[which] + (size_t)t0 * p.C8 + c8;
+  uint4* __restrict__ st = p.state[which] + (size_t)slot * NS * p.C8 + c8;
+  uint4* __restrict__ cache = p.cache[which] + c8;
   const int32_t* pt_row = p.page_table + (size_t)b * p.pt_stride;
 
-  // taps of this thread's 4 channels: 4 * W contiguous floats, read as W
+  // taps of this thread's 8 channels: 8 * W contiguous floats, read as 2 * W
   // 16-byte vectors when the tap array is 16-byte aligned
   float wt[kConvChan][W];
   {
-    const float* wp = p.w[which] + (size_t)c4 * kConvChan * W;
+    const float* wp = p.w[which] + (size_t)c8 * kConvChan * W;
     if ((reinterpret_cast<uintptr_t>(p.w[which]) & 15) == 0) {
 #pragma unroll
-      for (int v = 0; v < W; ++v) {
+      for (int v = 0; v < 2 * W; ++v) {
         const float4 f = __ldg(reinterpret_cast<const float4*>(wp) + v);
         wt[(4 * v) / W][(4 * v) % W] = f.x;
         wt[(4 * v + 1) / W][(4 * v + 1) % W] = f.y;
@@ -120,11 +125,11 @@ __global__ void __launch_bounds__(kConvThreads)
   }
 
   // the w-1 inputs before the segment: chunk-relative r = s0 - NS + j
-  uint2 win[NS > 0 ? NS : 1];
+  uint4 win[NS > 0 ? NS : 1];
 #pragma unroll
   for (int j = 0; j < NS; ++j) {
-    if (seg == 0) win[j] = st[(size_t)j * p.C4];  // r = j - NS < 0: state row j
-    else win[j] = __ldcs(x + (size_t)(s0 - NS + j) * p.C4);
+    if (seg == 0) win[j] = st[(size_t)j * p.C8];  // r = j - NS < 0: state row j
+    else win[j] = __ldcs(x + (size_t)(s0 - NS + j) * p.C8);
   }
 
   const int s1 = min(s0 + kConvSeg, q_len);
@@ -141,32 +146,32 @@ __global__ void __launch_bounds__(kConvThreads)
     const int page = __ldg(pt_row + lp);
     page_ok = page >= 0 && page < p.num_pages;
     if (!page_ok && threadIdx.x == 0) report(p.dev_err, INKLING_DEVERR_BAD_PAGE);
-    row0 = (size_t)page * p.P * p.C4;
+    row0 = (size_t)page * p.P * p.C8;
   };
   enter_page();
   for (int tb = s0; tb < s1; tb += kConvAhead) {
-    uint2 xin[kConvAhead];
+    uint4 xin[kConvAhead];
 #pragma unroll
     for (int u = 0; u < kConvAhead; ++u)
-      if (tb + u < s1) xin[u] = __ldcs(x + (size_t)(tb + u) * p.C4);
+      if (tb + u < s1) xin[u] = __ldcs(x + (size_t)(tb + u) * p.C8);
 #pragma unroll
     for (int u = 0; u < kConvAhead; ++u) {
       const int t = tb + u;
       if (t >= s1) break;
-      float acc[kConvChan] = {0.f, 0.f, 0.f, 0.f};
+      float acc[kConvChan];
+#pragma unroll
+      for (int c = 0; c < kConvChan; ++c) acc[c] = 0.f;
 #pragma unroll
       for (int j = 0; j < W; ++j) {
-        const float4 v = bf4_to_f4(j < NS ? win[j < NS ? j : 0] : xin[u]);
-        acc[0] = fmaf(wt[0][j], v.x, acc[0]);
-        acc[1] = fmaf(wt[1][j], v.y, acc[1]);
-        acc[2] = fmaf(wt[2][j], v.z, acc[2]);
-        acc[3] = fmaf(wt[3][j], v.w, acc[3]);
+        float v[8];
+        bf8_to_f8(j < NS ? win[j < NS ? j : 0] : xin[u], v);
+#pragma unroll
+        for (int c = 0; c < kConvChan; ++c) acc[c] = fmaf(wt[c][j], v[c], acc[c]);
       }
 #pragma unroll
       for (int j = 0; j + 1 < NS; ++j) win[j] = win[j + 1];
       if (NS > 0) win[NS > 0 ? NS - 1 : 0] = xin[u];
-      if (page_ok)
-        cache[row0 + (size_t)in_page * p.C4] = f4_to_bf4(make_float4(acc[0], acc[1], acc[2], acc[3]));
+      if (page_ok) cache[row0 + (size_t)in_page * p.C8] = f8_to_bf8(acc);
       if (++in_page == p.P && t + 1 < s1) {  // the next token starts the next logical page
         in_page = 0;
         ++lp;
@@ -182,24 +187,24 @@ __global__ void __launch_bounds__(kConvThreads)
   if (seg == 0) {
     if (q_len <= kConvSeg) {
 #pragma unroll
-      for (int j = 0; j < NS; ++j) st[(size_t)j * p.C4] = win[j];
+      for (int j = 0; j < NS; ++j) st[(size_t)j * p.C8] = win[j];
     } else {
 #pragma unroll
-      for (int j = 0; j < NS; ++j) st[(size_t)j * p.C4] = __ldcs(x + (size_t)(q_len - NS + j) * p.C4);
+      for (int j = 0; j < NS; ++j) st[(size_t)j * p.C8] = __ldcs(x + (size_t)(q_len - NS + j) * p.C8);
     }
   }
 }
 
 int launch_kv_conv_append(const KvConvCall& c) {
   KvConvParams prm;
-  prm.x[0] = static_cast<const uint2*>(c.k_new);
-  prm.x[1] = static_cast<const uint2*>(c.v_new);
+  prm.x[0] = static_cast<const uint4*>(c.k_new);
+  prm.x[1] = static_cast<const uint4*>(c.v_new);
   prm.w[0] = c.w_k;
   prm.w[1] = c.w_v;
-  prm.state[0] = static_cast<uint2*>(c.state_k);
-  prm.state[1] = static_cast<uint2*>(c.state_v);
-  prm.cache[0] = static_cast<uint2*>(c.k_cache);
-  prm.cache[1] = static_cast<uint2*>(c.v_cache);
+  prm.state[0] = static_cast<uint4*>(c.state_k);
+  prm.state[1] = static_cast<uint4*>(c.state_v);
+  prm.cache[0] = static_cast<uint4*>(c.k_cache);
+  prm.cache[1] = static_cast<uint4*>(c.v_cache);
   prm.cu = c.cu_seqlens_q;
   prm.seq_lens = c.seq_lens;
   prm.page_table = c.page_table;
@@ -211,11 +216,11 @@ int launch_kv_conv_append(const KvConvCall& c) {
   prm.P = c.P;
   prm.num_pages = c.num_pages;
   prm.num_slots = c.num_slots;
-  prm.C4 = c.H_kv * c.D / kConvChan;
+  prm.C8 = c.H_kv * c.D / kConvChan;
   prm.segs = (c.max_q_len + kConvSeg - 1) / kConvSeg;
   const int64_t gy = (int64_t)c.B * prm.segs;  // (sequence, segment) pairs
   if (gy <= 0 || gy > 65535) return INKLING_ERR_ARG;
-  const dim3 grid((prm.C4 + kConvThreads - 1) / kConvThreads, (unsigned)gy, 2);
+  const dim3 grid((prm.C8 + kConvThreads - 1) / kConvThreads, (unsigned)gy, 2);
   switch (c.width) {
     case 1: kv_conv_append_kernel<1><<<grid, kConvThreads, 0, c.stream>>>(prm); break;
     case 2: kv_conv_append_kernel<2><<<grid, kConvThreads, 0, c.stream>>>(prm); break;

@@ -11,13 +11,16 @@
 //    visible key range into a 3-stage ring, in page-respecting tiles of 64
 //    keys exactly like the decode kernel; warp 6 loads the V tiles the same
 //    way into a 2-stage ring (128-byte swizzle);
-//  * warp 7 loads the bias bands (below) into a 3-buffer ring;
-//  * warp 1 owns tensor memory (S double buffer 2 x 64 columns, and two O
+//  * warp 7 loads the bias bands (below) into a 3-buffer ring (L2
+//    evict-normal: consecutive tiles' bands share a 16-byte piece, which then
+//    comes from DRAM once);
+//  * warp 1 owns tensor memory (three S buffers of 64 columns, and two O
 //    accumulators of D columns, one per half of the key columns) and one of
 //    its threads issues the MMAs: S_k = Q K_k^T (A and B from shared memory,
-//    K-major) and O += P_{k-1} V_{k-1} (A = P from tensor memory, B = V
-//    MN-major from shared memory), so QK^T of tile k overlaps the softmax of
-//    tile k-1;
+//    K-major) and O += P_k V_k (A = P from tensor memory, B = V MN-major from
+//    shared memory).  S_0 and S_1 go first; then, as soon as P_k is written,
+//    PV_k is issued interleaved with S_{k+2}, so the QK^T of a tile is ready a
+//    whole softmax ahead.  Its shared-memory descriptors are computed once;
 //  * warps 2-5 and 8-11 are two softmax warpgroups sharing every row: a
 //    thread owns one query row (one TMEM lane) and one half of the key
 //    columns of each tile.  It reads S with tcgen05.ld, adds the bias, applies
@@ -25,7 +28,11 @@
 //    rescaled in tensor memory only when the max grows by more than 2^8) and
 //    writes P (bf16) back over its S columns with tcgen05.st; the epilogue
 //    merges the two halves and stores the normalised output (full tiles
-//    through shared memory and TMA).
+//    through shared memory and TMA).  The scores, exponent arguments and row
+//    sums use packed fp32 pairs (fma / add .f32x2), the row max three-input
+//    max.
+// Every mbarrier wait lets the hardware suspend the waiting warp until the
+// phase completes instead of polling (a suspend-time hint).
 //
 // The bias is the dominant HBM stream: every query row reads its own band of
 // rel_logits, 64 distances per key tile, each element exactly once.  Rows are
@@ -54,6 +61,7 @@ constexpr int kQRows = 128;
 constexpr int kKStages = 3;  // K tiles: released when QK^T has read them
 constexpr int kVStages = 2;  // V tiles: released when PV has read them
 constexpr int kBiasBufs = 3;
+constexpr int kSBufs = 3;  // S tiles in tensor memory: S_k is computed while softmax k-1 and k-2 run
 constexpr int kBiasPitch = 68;                       // floats per row band (64 + alignment)
 constexpr int kBiasWarpBytes = 32 * kBiasPitch * 4;  // 32 rows of one warp
 constexpr int kBiasBufBytes = 4 * kBiasWarpBytes;    // 128 rows
@@ -91,9 +99,89 @@ struct PrefillSmem {
   static constexpr int BAR_OFF = X_OFF + 2 * 2 * kQRows * 4;
   // q_full, k_full/empty, v_full/empty, s_full[2], p_full[2], pv_done, b_full/empty, x_bar[4],
   // o_done
-  static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 2 * kBiasBufs + 4 + 1;
+  static constexpr int NBARS = 1 + 2 * kKStages + 2 * kVStages + 3 * kSBufs + 2 * kBiasBufs + 4 + 1;
   static constexpr int TOTAL = BAR_OFF + NBARS * 8 + 16;
 };
+
+// L2 policy of the bias loads: evict-normal (an evict-first line holding the
+// 16 bytes that two consecutive key tiles' bands share is gone before the
+// second band is loaded, and is then read from DRAM twice)
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// mbarrier waits that let the hardware suspend the warp (up to kSuspendNs)
+// until the phase completes, instead of polling.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_s(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait_s(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait_s(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (__all_sync(0xffffffffu, mbar_try_wait_s(bar, parity))) return true;
+  const unsigned long long t0 = globaltimer();
+  const bool leader = (threadIdx.x & 31) == 0;
+  for (;;) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_s(bar, parity))) return true;
+    int stop = 0;
+    if (leader) {
+      if (*abort) {
+        stop = 1;
+      } else if (globaltimer() - t0 > kWaitTimeoutNs) {
+        *abort = 1;
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+  }
+}
+
+// Packed fp32 pairs (two lanes of one 64-bit register, .x in the low half):
+// fma / add on both halves in one instruction, rounding as two fma.rn / add.rn.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (NaN operands ignored, as fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 // Scores of one column half (32 keys) of a 64-key tile for one query row:
 // s[cc] = scale * S[cc] + bias, the bias read from the row's band in shared
@@ -114,8 +202,12 @@ __device__ __forceinline__ void half_scores(float (&s)[32], const uint32_t (&sra
     bb[4 * q + 2] = v.z;
     bb[4 * q + 3] = v.w;
   }
+  const uint64_t sc2 = f2_pack(scale, scale);
 #pragma unroll
-  for (int cc = 0; cc < 32; ++cc) s[cc] = fmaf(__uint_as_float(sraw[cc]), scale, bb[OFF + 31 - cc]);
+  for (int cc = 0; cc < 32; cc += 2)
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sraw[cc]), __uint_as_float(sraw[cc + 1])), sc2,
+                     f2_pack(bb[OFF + 31 - cc], bb[OFF + 30 - cc])),
+              s[cc], s[cc + 1]);
 }
 
 template <int D, int BH>
@@ -127,7 +219,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   // S0 [0,64) S1 [64,128); O_A [128, 128+D) accumulates key columns 0..31 of
   // every tile, O_B [256, 256+D) columns 32..63 (merged in the epilogue)
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kOCol = 128;
+  constexpr uint32_t kOCol = 64 * kSBufs;
   constexpr uint32_t kOHalfStride = 128;
 
   extern __shared__ uint8_t smem_raw[];
@@ -155,9 +247,9 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   uint64_t* v_full = k_empty + kKStages;
   uint64_t* v_empty = v_full + kVStages;
   uint64_t* s_full = v_empty + kVStages;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* b_full = pv_done + 1;
+  uint64_t* p_full = s_full + kSBufs;   // one barrier per S buffer: phases are
+  uint64_t* pv_done = p_full + kSBufs;  // kSBufs tiles apart, parity waits stay exact
+  uint64_t* b_full = pv_done + kSBufs;
   uint64_t* b_empty = b_full + kBiasBufs;
   uint64_t* x_bar = b_empty + kBiasBufs;  // per lane group: the two softmax warps of a row
   // every MMA of the CTA has completed (one phase, committed after the last PV).
@@ -178,12 +270,12 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSBufs; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&p_full[s]), 8);  // the eight softmax warps
+      mbar_init(smem_u32(&pv_done[s]), 1);
     }
     for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&x_bar[s]), 2);
-    mbar_init(smem_u32(pv_done), 1);
     mbar_init(smem_u32(o_done), 1);
     for (int s = 0; s < kBiasBufs; ++s) {
       mbar_init(smem_u32(&b_full[s]), 1);   // the bias loader warp
@@ -280,7 +372,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       while (!plan.done()) {
         const int st = kt % nst;
         if (kt >= nst && lane == 0)
-          ok = mbar_wait(smem_u32(&empty[st]), ((kt / nst) - 1) & 1, abort_flag);
+          ok = wait1(smem_u32(&empty[st]), ((kt / nst) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         int lp, slot0;
@@ -302,7 +394,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       while (!plan.done()) {
         const int st = kt % nst;
         if (kt >= nst && lane == 0)
-          ok = mbar_wait(smem_u32(&empty[st]), ((kt / nst) - 1) & 1, abort_flag);
+          ok = wait1(smem_u32(&empty[st]), ((kt / nst) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const Tile t = plan.next();
@@ -346,28 +438,8 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16(kQRows, kTileRows, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kQRows, D, true);
       const uint32_t q_base = smem_u32(smem);
-      bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag);
+      bool ok = wait1(smem_u32(q_full), 0, abort_flag);
       tc_fence_after();
-      auto issue_pv = [&](int kp) -> bool {
-        if (!mbar_wait(smem_u32(&p_full[kp & 1]), (kp >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const int st = kp % kVStages;
-        if (!mbar_wait(smem_u32(&v_full[st]), (kp / kVStages) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(smem + SM::V_OFF + st * TILE_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {  // keys 16kk..16kk+15
-          const uint64_t bdesc = smem_desc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
-          // keys 0..31 -> O_A with P at S columns 0..15; keys 32..63 -> O_B with
-          // P at S columns 32..47
-          const uint32_t o = tmem + kOCol + (kk >= 2 ? kOHalfStride : 0);
-          const uint32_t a = tmem + 64 * (kp & 1) + (kk >= 2 ? 32 + 8 * (kk - 2) : 8 * kk);
-          tc_mma_ts(o, a, bdesc, idesc_pv, (kp > 0 || (kk & 1)) ? 1u : 0u);
-        }
-        tc_commit(smem_u32(pv_done));
-        tc_commit(smem_u32(&v_empty[st]));
-        return true;
-      };
       int k = 0;
       if (ok) {
         // walk the same tiles as the loader (only the count matters here)
@@ -386,29 +458,75 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
             ++ntiles;
           }
         }
-        for (k = 0; k < ntiles && ok; ++k) {
-          const int st = k % kKStages;
-          ok = mbar_wait(smem_u32(&k_full[st]), (k / kKStages) & 1, abort_flag);
+        // Shared-memory descriptors, computed once: a descriptor's start
+        // address field is bits 0..13 of (address >> 4), so the descriptor of
+        // base + off is that of base plus off >> 4 (all offsets stay inside
+        // shared memory: no carry out of the field).
+        const uint64_t q_desc0 = smem_desc_sw128(q_base, 16, 1024);
+        const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + SM::K_OFF), 16, 1024);
+        const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + SM::V_OFF), kHalfBytes, 1024);
+        // One MMA of S_kn = Q K_kn^T (k-step kk, into S buffer kn % kSBufs).
+        auto s_mma = [&](int kn, int kk) {
+          const uint32_t koff = (uint32_t)((kn % kKStages) * TILE_BYTES) >> 4;
+          const uint64_t adesc = q_desc0 + (uint32_t)(((kk >> 2) * SM::QHALF + (kk & 3) * 32) >> 4);
+          const uint64_t bdesc =
+              k_desc0 + koff + (uint32_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + 64 * (kn % kSBufs), adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+        };
+        // S_kn may start once K_kn is in and its buffer's previous P
+        // (P_{kn - kSBufs}) has been read by its PV
+        auto s_ready = [&](int kn) -> bool {
+          if (!wait1(smem_u32(&k_full[kn % kKStages]), (kn / kKStages) & 1, abort_flag)) return false;
+          if (kn >= kSBufs) {
+            const int kq = kn - kSBufs;
+            if (!wait1(smem_u32(&pv_done[kq % kSBufs]), (kq / kSBufs) & 1, abort_flag)) return false;
+          }
+          return true;
+        };
+        // S_0 and S_1 ahead, then at each step k (once P_k is written): PV_k
+        // interleaved with S_{k+2}.  Consecutive MMAs of one accumulator wait
+        // on each other; MMAs of different accumulators (O_A, O_B, S) overlap,
+        // so the PVs run in the gaps of the S chain, and S_{k+2} is ready a
+        // whole softmax ahead.
+        for (int kn = 0; kn < 2 && kn < ntiles && ok; ++kn) {
+          ok = s_ready(kn);
           if (!ok) break;
-          if (k >= 2) {  // S buffer k&1 is free once PV_{k-2} has read P_{k-2}
-            ok = mbar_wait(smem_u32(pv_done), (k - 2) & 1, abort_flag);
-            if (!ok) break;
-          }
           tc_fence_after();
-          const uint32_t kb = smem_u32(smem + SM::K_OFF + st * TILE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t adesc =
-                smem_desc_sw128(q_base + (kk >> 2) * SM::QHALF + (kk & 3) * 32, 16, 1024);
-            const uint64_t bdesc =
-                smem_desc_sw128(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-            tc_mma_ss(tmem + 64 * (k & 1), adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&s_full[k & 1]));
-          tc_commit(smem_u32(&k_empty[st]));
-          if (k >= 1) ok = issue_pv(k - 1);
+          for (int kk = 0; kk < D / 16; ++kk) s_mma(kn, kk);
+          tc_commit(smem_u32(&s_full[kn % kSBufs]));
+          tc_commit(smem_u32(&k_empty[kn % kKStages]));
         }
-        if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
+        for (k = 0; k < ntiles && ok; ++k) {
+          const int kn = k + 2;
+          const bool do_s = kn < ntiles;
+          ok = wait1(smem_u32(&p_full[k % kSBufs]), (k / kSBufs) & 1, abort_flag);
+          if (ok) ok = wait1(smem_u32(&v_full[k % kVStages]), (k / kVStages) & 1, abort_flag);
+          if (ok && do_s) ok = s_ready(kn);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t v_desc = v_desc0 + ((uint32_t)((k % kVStages) * TILE_BYTES) >> 4);
+          // PV_k: keys 0..31 -> O_A (P at S columns 0..15), keys 32..63 -> O_B
+          // (P at S columns 32..47), key blocks in the order 0, 2, 1, 3, each
+          // after one MMA of S_{k+2}
+#pragma unroll
+          for (int j = 0; j < kTileRows / 16; ++j) {
+            if (do_s) s_mma(kn, j);
+            const int kk = (j >> 1) | ((j & 1) << 1);
+            const uint64_t bdesc = v_desc + (uint32_t)((kk * 16 * 128) >> 4);
+            const uint32_t o = tmem + kOCol + (kk >= 2 ? kOHalfStride : 0);
+            const uint32_t a = tmem + 64 * (k % kSBufs) + (kk >= 2 ? 32 + 8 * (kk - 2) : 8 * kk);
+            tc_mma_ts(o, a, bdesc, idesc_pv, (k > 0 || (kk & 1)) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&pv_done[k % kSBufs]));
+          tc_commit(smem_u32(&v_empty[k % kVStages]));
+          if (do_s) {
+#pragma unroll
+            for (int kk = kTileRows / 16; kk < D / 16; ++kk) s_mma(kn, kk);
+            tc_commit(smem_u32(&s_full[kn % kSBufs]));
+            tc_commit(smem_u32(&k_empty[kn % kKStages]));
+          }
+        }
       }
       tc_commit(smem_u32(o_done));  // arrives once every MMA issued above has completed
       if (!ok) {
@@ -460,16 +578,16 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       } else {
         t = cur.next();
       }
-      if (!mbar_wait_warp(smem_u32(&s_full[k & 1]), (k >> 1) & 1, abort_flag)) {
+      if (!waitw(smem_u32(&s_full[k % kSBufs]), (k / kSBufs) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sraw[32];
-      tmem_ld32(tlane + 64 * (k & 1) + c0, sraw);
+      tmem_ld32(tlane + 64 * (k % kSBufs) + c0, sraw);
       tmem_ld_wait();
       const int buf = k % kBiasBufs;
-      if (!mbar_wait_warp(smem_u32(&b_full[buf]), (k / kBiasBufs) & 1, abort_flag)) {
+      if (!waitw(smem_u32(&b_full[buf]), (k / kBiasBufs) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -515,14 +633,13 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
 
       float mx;
       {
-        float r16[16];
+        float r11[11];  // 32 -> 11 -> 4 -> 1 with three-input max
 #pragma unroll
-        for (int j = 0; j < 16; ++j) r16[j] = fmaxf(s[j], s[j + 16]);
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w; ++j) r16[j] = fmaxf(r16[j], r16[j + w]);
-        mx = r16[0];
+        for (int j = 0; j < 10; ++j) r11[j] = fmax3(s[3 * j], s[3 * j + 1], s[3 * j + 2]);
+        r11[10] = fmaxf(s[30], s[31]);
+        const float r0 = fmax3(r11[0], r11[1], r11[2]), r1 = fmax3(r11[3], r11[4], r11[5]);
+        const float r2 = fmax3(r11[6], r11[7], r11[8]), r3 = fmaxf(r11[9], r11[10]);
+        mx = fmax3(r0, r1, fmaxf(r2, r3));
       }
       float m_new = m_use, alpha = 1.f;
       bool resc = false;
@@ -537,7 +654,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       }
       if (__any_sync(0xffffffffu, resc)) {
         // my O holds PV_0..PV_{k-1}; wait for the last one, then rescale it
-        if (!mbar_wait_warp(smem_u32(pv_done), (k - 1) & 1, abort_flag)) {
+        if (!waitw(smem_u32(&pv_done[(k - 1) % kSBufs]), ((k - 1) / kSBufs) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -557,29 +674,31 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       l_part *= alpha;
       const float nmu = (m_use == -INFINITY) ? 0.f : -m_use * kLog2e;
       uint32_t pk[16];
-      float ps[16];
+      {
+        const uint64_t l2e2 = f2_pack(kLog2e, kLog2e), nmu2 = f2_pack(nmu, nmu);
+        uint64_t acc[4] = {0, 0, 0, 0};  // four packed partial sums (+0.0 bits)
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float p0 = ex2(fmaf(s[2 * m], kLog2e, nmu));
-        const float p1 = ex2(fmaf(s[2 * m + 1], kLog2e, nmu));
-        ps[m] = p0 + p1;
-        pk[m] = pack_bf16(p0, p1);
+        for (int m = 0; m < 16; ++m) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(s[2 * m], s[2 * m + 1]), l2e2, nmu2), a0, a1);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          acc[m & 3] = f2_add(acc[m & 3], f2_pack(p0, p1));
+          pk[m] = pack_bf16(p0, p1);
+        }
+        float u0, u1;
+        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), u0, u1);
+        l_part += u0 + u1;
       }
-#pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
-      l_part += ps[0];
       // my half of P (16 bf16 pairs) over the first 16 of my own S columns
       // (which I have already read): half A at columns 0..15, half B at 32..47
-      tmem_st16(tlane + 64 * (k & 1) + c0, pk);
+      tmem_st16(tlane + 64 * (k % kSBufs) + c0, pk);
       tmem_st_wait();
 
       if (t.dirty) {
         // rows outside [klo, khi] may hold other keys' values (NaN included):
         // zero them in V so that P = 0 times V stays 0 in the tensor core
         const int st = k % kVStages;
-        if (!mbar_wait_warp(smem_u32(&v_full[st]), (k / kVStages) & 1, abort_flag)) {
+        if (!waitw(smem_u32(&v_full[st]), (k / kVStages) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -597,18 +716,18 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full[k & 1]));
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[k % kSBufs]));
     }
 
     // ---- epilogue: merge the two halves, O / l -> bf16 (half the columns each)
-    if (ok && k > 0) ok = mbar_wait_warp(smem_u32(o_done), 0, abort_flag);
+    if (ok && k > 0) ok = waitw(smem_u32(o_done), 0, abort_flag);
     float M = m_use, L = l_part, sc_a = 1.f, sc_b = 0.f;
     if (ok) {
       xbuf[(0 * 2 + grp) * 128 + i] = m_use;
       xbuf[(1 * 2 + grp) * 128 + i] = l_part;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&x_bar[lg]));
-      ok = mbar_wait_warp(smem_u32(&x_bar[lg]), 0, abort_flag);
+      ok = waitw(smem_u32(&x_bar[lg]), 0, abort_flag);
       if (ok) {
         const float ma = xbuf[(0 * 2 + 0) * 128 + i], mb = xbuf[(0 * 2 + 1) * 128 + i];
         const float la = xbuf[(1 * 2 + 0) * 128 + i], lb = xbuf[(1 * 2 + 1) * 128 + i];
@@ -682,7 +801,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
     // Within a group the band start moves by exactly 4 floats per row, so one
     // TMA box of a sheared view (token stride plus 4 floats per row) loads the
     // whole group.
-    const uint64_t pol_b = policy_evict_first();
+    const uint64_t pol_b = policy_evict_normal();
     using PlanT = typename std::conditional<BH == 64, PlanBig, PlanSmall>::type;
     PlanT pl = [&]() {
       if constexpr (BH == 64) return PlanBig(klo_all, khi_all, p.P);
@@ -701,7 +820,7 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       }
       const int buf = k % kBiasBufs;
       if (k >= kBiasBufs &&
-          !mbar_wait_warp(smem_u32(&b_empty[buf]), ((k / kBiasBufs) - 1) & 1, abort_flag)) {
+          !waitw(smem_u32(&b_empty[buf]), ((k / kBiasBufs) - 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
