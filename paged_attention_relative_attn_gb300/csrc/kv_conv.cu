@@ -11,13 +11,15 @@
 // by the last w-1 inputs of this call.  The convolved rows are written into
 // the paged cache at the tokens' positions (as inkling_rel_attn_kv_append).
 //
-// Grid: x = channel blocks of 8 * 128 channels, y = (sequence, segment of 64
-// new tokens), z = K or V: small CTAs, many of them, so that the last wave is
-// short.  A thread owns 8 adjacent channels (16-byte loads and stores, 512
-// contiguous bytes per warp and token), keeps the last w-1 inputs in registers
-// and walks its segment's tokens in order, loading eight tokens ahead; the
-// cache slot advances with the position (one page-table read per page
-// crossed, no division per token).  Only the first segment of a sequence reads the old state
+// Grid: x = channel blocks of 8 * 64 channels, y = (sequence, segment of 64
+// new tokens), z = K or V: small CTAs, many of them, all resident at once.  A
+// thread owns 8 adjacent channels (16-byte loads and stores, 512 contiguous
+// bytes per warp and token), keeps the last w-1 inputs in registers and walks
+// its segment's tokens in order.  Its input rows arrive through a private
+// shared-memory ring: while token t is convolved, the 16-byte row of token
+// t + 6 is being copied (cp.async, one commit group per token), so six rows
+// stay in flight without holding registers.  The cache slot advances with the
+// position (one page-table read per page crossed, no division per token).  Only the first segment of a sequence reads the old state
 // (later segments start w-1 tokens back inside the new tokens, since a segment
 // is longer than any window), and the same thread that read a channel's old
 // state writes its new one -- so the pool row is updated in place without a
@@ -31,10 +33,21 @@
 
 namespace ira {
 
-constexpr int kConvThreads = 128;
+constexpr int kConvThreads = 64;
 constexpr int kConvSeg = 64;     // new tokens per CTA (>= the widest window)
-constexpr int kConvAhead = 8;    // tokens loaded ahead per thread
 constexpr int kConvChan = 8;     // channels per thread
+constexpr int kRingSlots = 8;    // shared-memory ring slots per thread (one token row each)
+constexpr int kRingAhead = 6;    // token rows in flight per thread
+
+// 16-byte global -> shared copies (L2 only), committed and waited on per token
+__device__ __forceinline__ void ring_copy(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void ring_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void ring_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 struct KvConvParams {
   const uint4* x[2];       // k_new, v_new: [T][C / 8] of 8 x bf16
@@ -149,36 +162,50 @@ __global__ void __launch_bounds__(kConvThreads)
     row0 = (size_t)page * p.P * p.C8;
   };
   enter_page();
-  for (int tb = s0; tb < s1; tb += kConvAhead) {
-    uint4 xin[kConvAhead];
+  // rolling prefetch: token t + kRingAhead is copied into this thread's slot
+  // of a shared-memory ring while token t is convolved (one commit group per
+  // token, so the wait for token t leaves kRingAhead copies in flight)
+  __shared__ uint4 ring[kRingSlots][kConvThreads];
+  const uint32_t my_slot0 = (uint32_t)__cvta_generic_to_shared(&ring[0][threadIdx.x]);
+  constexpr uint32_t kSlotStride = kConvThreads * 16;
 #pragma unroll
-    for (int u = 0; u < kConvAhead; ++u)
-      if (tb + u < s1) xin[u] = __ldcs(x + (size_t)(tb + u) * p.C8);
+  for (int u = 0; u < kRingAhead; ++u) {
+    if (s0 + u < s1) ring_copy(my_slot0 + u * kSlotStride, x + (size_t)(s0 + u) * p.C8);
+    ring_commit();
+  }
+  int rs = 0;  // ring slot of token t
+  for (int t = s0; t < s1; ++t) {
+    {
+      const int tn = t + kRingAhead;
+      int sn = rs + kRingAhead;
+      sn = sn >= kRingSlots ? sn - kRingSlots : sn;
+      if (tn < s1) ring_copy(my_slot0 + sn * kSlotStride, x + (size_t)tn * p.C8);
+      ring_commit();
+    }
+    ring_wait<kRingAhead>();
+    const uint4 xt = ring[rs][threadIdx.x];
+    rs = rs + 1 == kRingSlots ? 0 : rs + 1;
+    float acc[kConvChan];
 #pragma unroll
-    for (int u = 0; u < kConvAhead; ++u) {
-      const int t = tb + u;
-      if (t >= s1) break;
-      float acc[kConvChan];
+    for (int c = 0; c < kConvChan; ++c) acc[c] = 0.f;
 #pragma unroll
-      for (int c = 0; c < kConvChan; ++c) acc[c] = 0.f;
+    for (int j = 0; j < W; ++j) {
+      float v[8];
+      bf8_to_f8(j < NS ? win[j < NS ? j : 0] : xt, v);
 #pragma unroll
-      for (int j = 0; j < W; ++j) {
-        float v[8];
-        bf8_to_f8(j < NS ? win[j < NS ? j : 0] : xin[u], v);
+      for (int c = 0; c < kConvChan; ++c) acc[c] = fmaf(wt[c][j], v[c], acc[c]);
+    }
 #pragma unroll
-        for (int c = 0; c < kConvChan; ++c) acc[c] = fmaf(wt[c][j], v[c], acc[c]);
-      }
-#pragma unroll
-      for (int j = 0; j + 1 < NS; ++j) win[j] = win[j + 1];
-      if (NS > 0) win[NS > 0 ? NS - 1 : 0] = xin[u];
-      if (page_ok) cache[row0 + (size_t)in_page * p.C8] = f8_to_bf8(acc);
-      if (++in_page == p.P && t + 1 < s1) {  // the next token starts the next logical page
-        in_page = 0;
-        ++lp;
-        enter_page();
-      }
+    for (int j = 0; j + 1 < NS; ++j) win[j] = win[j + 1];
+    if (NS > 0) win[NS > 0 ? NS - 1 : 0] = xt;
+    if (page_ok) cache[row0 + (size_t)in_page * p.C8] = f8_to_bf8(acc);
+    if (++in_page == p.P && t + 1 < s1) {  // the next token starts the next logical page
+      in_page = 0;
+      ++lp;
+      enter_page();
     }
   }
+  ring_wait<0>();
 
   // new state: the last w-1 inputs of the sequence.  When all its new tokens
   // fall in this first segment, the window now holds exactly those (it began
