@@ -27,7 +27,10 @@
 //    (the producer prefetches each item's rel_logits rows there; each tile's
 //    values are loaded one tile ahead), mask, and keep an online softmax per
 //    row with warp shuffles over the keys.  P goes from the accumulator layout
-//    to the B-operand layout with movmatrix.  At the end of an item the four
+//    to the B-operand layout with movmatrix.  With one n-tile the q fragments
+//    stay in registers for the whole item; with two they are read from the
+//    item's shared-memory slot (rows padded to 272 bytes, one ldmatrix per
+//    k-step), which keeps the two-n-tile consumer inside its registers.  At the end of an item the four
 //    warps' (m, l, O) are combined through shared memory (one buffer per warp,
 //    or two buffers in two rounds where that leaves room for a third stage)
 //    and written as the final bf16 output or, when the sequence spans several
@@ -147,7 +150,11 @@ struct DecodeSmem {
   __host__ __device__ DecodeSmem(int D, int G, int NT, int stages_, int n_prefix, int comb_slots) {
     stage_bytes = 2 * (D / 64) * kHalfBytes;
     stages = stages_;
-    slot_bytes = 128 + ((G * D * 2 + 127) / 128) * 128;  // item record + q rows
+    // item record + q rows; with two n-tiles the rows are padded by 16 bytes
+    // (read by ldmatrix per k-step: eight rows then fall in distinct banks)
+    const int qpitch = NT == 2 ? D * 2 + 16 : D * 2;
+    const int qrows = NT == 2 ? 16 : G;  // two n-tiles: ldmatrix reads all 16 rows
+    slot_bytes = 128 + ((qrows * qpitch + 127) / 128) * 128;
     ring_off = stages * stage_bytes;
     comb_off = ring_off + kItemSlots * slot_bytes;
     const int comb_bytes = comb_slots * G * (D + 4) * 4 + 2 * kConsumerWarps * 8 * NT * 4;
@@ -175,6 +182,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
   // one n-tile of multi-token rows the vote costs more than it saves.
   constexpr bool kLazyRescale = !(MULTI && NT == 1);
   constexpr int HP = 8 * NT;  // padded heads per group
+  // Two n-tiles: the q fragments are read from the item slot at every k-step
+  // (ldmatrix) instead of being held in 32 registers for the whole item, and
+  // the slot is released when the item's last QK^T is done.
+  constexpr bool kQSmem = NT == 2;
+  constexpr int QP = kQSmem ? D * 2 + 16 : D * 2;  // bytes per q row in a slot
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -215,6 +227,13 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     }
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if constexpr (kQSmem) {
+    for (int i = tid; i < kItemSlots * (L.slot_bytes - 128) / 16; i += kDecodeThreads) {
+      const int s = i / ((L.slot_bytes - 128) / 16), o = i - s * ((L.slot_bytes - 128) / 16);
+      *reinterpret_cast<uint4*>(slot_q(s) + 16 * o) = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
 
@@ -347,7 +366,16 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         if (r.b >= 0 && r.nvis > 0) {
           // q rows (token i, head gh) in order i * G + gh: one copy per token
           const uint32_t tbytes = G * D * 2;
-          if constexpr (MULTI) {
+          if constexpr (kQSmem) {  // one copy per row, at the padded pitch
+            const int ntok = MULTI ? r.tn : 1;
+            mbar_arrive_expect_tx(fb, ntok * tbytes);
+            for (int i = 0; i < ntok; ++i) {
+              const size_t tok = MULTI ? (size_t)(r.t0 + i) : (size_t)r.b;
+              for (int gh = 0; gh < G; ++gh)
+                bulk_load(smem_u32(slot_q(slot)) + (i * G + gh) * QP,
+                          p.q + (tok * p.H_q + r.hkv * G + gh) * D, D * 2, fb);
+            }
+          } else if constexpr (MULTI) {
             mbar_arrive_expect_tx(fb, r.tn * tbytes);
             for (int i = 0; i < r.tn; ++i)
               bulk_load(smem_u32(slot_q(slot)) + i * tbytes,
@@ -543,8 +571,9 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     const ItemRec r = *slot_rec(slot);
     const bool final_out = r.n_s <= 1;
     const int NRi = MULTI ? r.tn * G : G;  // live rows of this item
-    uint32_t qf[KS][NT][2];
-    if (r.b >= 0 && r.nvis > 0) {
+    uint32_t qf[kQSmem ? 1 : KS][NT][2];
+    const uint32_t q_smem = smem_u32(slot_q(slot));
+    if (!kQSmem && r.b >= 0 && r.nvis > 0) {
       const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(slot_q(slot));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -552,14 +581,19 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         const bool live = head < NRi;
         const __nv_bfloat16* qrow = qs + (live ? head : 0) * D;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
+        for (int ks = 0; ks < (kQSmem ? 0 : KS); ++ks) {
           qf[ks][nt][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4) : 0u;
           qf[ks][nt][1] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8) : 0u;
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));  // slot free: q is in registers
+    // slot free: q is in registers (two n-tiles: once the item's QK^T is done)
+    auto release_slot = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rempty[slot]));
+    };
+    if (!kQSmem || r.b < 0) release_slot();
     if (r.b < 0) break;
 
     // output row of item row rr = (token i, head gh)
@@ -571,6 +605,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
         return (size_t)r.b * p.H_q + r.hkv * G + rr;
       }
     };
+    if (kQSmem && (r.nvis == 0 || (MULTI && r.a > r.e))) release_slot();
     if (r.nvis == 0) {  // nothing visible: out = 0, lse = -inf
       for (int i = tid; i < NRi * D; i += kConsumerThreads) {
         const int rr = i / D, d = i - rr * D;
@@ -689,12 +724,26 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
             kb + (chunk >> 3) * kHalfBytes + k_row * 128 + (((chunk & 7) ^ sw) << 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4(addr, a0, a1, a2, a3);
+        uint32_t b[NT][2];
+        if constexpr (kQSmem) {
+          // rows (lane & 7) + 8 (lane >> 4), columns 16 ks + 8 ((lane >> 3) & 1):
+          // registers = rows 0-7 / 8-15 at k = 2 c4 and 2 c4 + 8
+          const uint32_t qa = q_smem + ((lane & 7) + 8 * (lane >> 4)) * QP + 32 * ks +
+                              16 * ((lane >> 3) & 1);
+          ldsm_x4(qa, b[0][0], b[0][1], b[NT - 1][0], b[NT - 1][1]);
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            b[nt][0] = qf[kQSmem ? 0 : ks][nt][0];
+            b[nt][1] = qf[kQSmem ? 0 : ks][nt][1];
+          }
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (kTwoChains && (ks & 1))
-            mma_16816(sacc2[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+            mma_16816(sacc2[nt], a0, a1, a2, a3, b[nt][0], b[nt][1]);
           else
-            mma_16816(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+            mma_16816(sacc[nt], a0, a1, a2, a3, b[nt][0], b[nt][1]);
         }
       }
       if constexpr (kTwoChains) {
@@ -835,6 +884,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       PlanSmall plan(r.a, r.e);
       ok = run_tiles(plan, [](PlanSmall& pl) { return pl.next(); });
     }
+    if (kQSmem) release_slot();
     if (!ok) break;
 
     // ---- finish the item: sum l over the lanes of the 16 keys

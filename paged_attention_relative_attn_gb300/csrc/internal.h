@@ -111,15 +111,16 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, vo
 // sequence and G query heads per KV head -- the rows (token, head) of an item
 // fill at most 16 (two 8-row MMA tiles).  Shared by the ABI helpers and the
 // launcher so that the split plan and the kernel agree.
-// (one 8-row MMA tile when it still holds two tokens of the group: the math
-// per key halves while each K/V tile is read once per two tokens; else two
-// tiles.  INKLING_MTP_MAX_ROWS > 0 forces the bound.)
+// (as many tokens as fit 16 rows: each K/V tile then passes through shared
+// memory and the MMAs once for all of them -- for 4 tokens x 3 heads one
+// 12-row item instead of two 6-row items.  INKLING_MTP_MAX_ROWS > 0 forces the
+// bound.)
 #ifndef INKLING_MTP_MAX_ROWS
 #define INKLING_MTP_MAX_ROWS 0
 #endif
 inline int32_t decode_token_group(int32_t q_len, int32_t G) {
   if (q_len <= 1) return 1;
-  const int32_t rows = INKLING_MTP_MAX_ROWS > 0 ? INKLING_MTP_MAX_ROWS : (2 * G <= 8 ? 8 : 16);
+  const int32_t rows = INKLING_MTP_MAX_ROWS > 0 ? INKLING_MTP_MAX_ROWS : 16;
   int32_t tg = G > 0 ? rows / G : 1;
   if (tg < 1) tg = 1;
   return tg < q_len ? tg : q_len;
