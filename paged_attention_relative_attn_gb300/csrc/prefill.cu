@@ -18,9 +18,10 @@
 //    accumulators of D columns, one per half of the key columns) and one of
 //    its threads issues the MMAs: S_k = Q K_k^T (A and B from shared memory,
 //    K-major) and O += P_k V_k (A = P from tensor memory, B = V MN-major from
-//    shared memory).  S_0 and S_1 go first; then, as soon as P_k is written,
-//    PV_k is issued interleaved with S_{k+2}, so the QK^T of a tile is ready a
-//    whole softmax ahead.  Its shared-memory descriptors are computed once;
+//    shared memory).  S_0, S_1 and S_2 go first; then, as soon as P_k is
+//    written, PV_k is issued, and once PV_k has completed, S_{k+3} into the
+//    buffer it has just read, so the QK^T of a tile is ready two softmax
+//    periods ahead.  Its shared-memory descriptors are computed once;
 //  * warps 2-5 and 8-11 are two softmax warpgroups sharing every row: a
 //    thread owns one query row (one TMEM lane) and one half of the key
 //    columns of each tile.  It reads S with tcgen05.ld, adds the bias, applies
@@ -61,7 +62,7 @@ constexpr int kQRows = 128;
 constexpr int kKStages = 3;  // K tiles: released when QK^T has read them
 constexpr int kVStages = 2;  // V tiles: released when PV has read them
 constexpr int kBiasBufs = 3;
-constexpr int kSBufs = 3;  // S tiles in tensor memory: S_k is computed while softmax k-1 and k-2 run
+constexpr int kSBufs = 3;  // S tiles in tensor memory: S_{k+3} is computed while softmax k+1 and k+2 run
 constexpr int kBiasPitch = 68;                       // floats per row band (64 + alignment)
 constexpr int kBiasWarpBytes = 32 * kBiasPitch * 4;  // 32 rows of one warp
 constexpr int kBiasBufBytes = 4 * kBiasWarpBytes;    // 128 rows
@@ -216,8 +217,9 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   using SM = PrefillSmem<D>;
   constexpr int HALVES = SM::HALVES;
   constexpr int TILE_BYTES = SM::TILE_BYTES;
-  // S0 [0,64) S1 [64,128); O_A [128, 128+D) accumulates key columns 0..31 of
-  // every tile, O_B [256, 256+D) columns 32..63 (merged in the epilogue)
+  // S buffers [0, 64 * kSBufs); O_A [kOCol, kOCol + D) accumulates key columns
+  // 0..31 of every tile, O_B [kOCol + 128, ...) columns 32..63 (merged in the
+  // epilogue)
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kOCol = 64 * kSBufs;
   constexpr uint32_t kOHalfStride = 128;
@@ -483,12 +485,10 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
           }
           return true;
         };
-        // S_0 and S_1 ahead, then at each step k (once P_k is written): PV_k
-        // interleaved with S_{k+2}.  Consecutive MMAs of one accumulator wait
-        // on each other; MMAs of different accumulators (O_A, O_B, S) overlap,
-        // so the PVs run in the gaps of the S chain, and S_{k+2} is ready a
-        // whole softmax ahead.
-        for (int kn = 0; kn < 2 && kn < ntiles && ok; ++kn) {
+        // S_0, S_1 and S_2 ahead; then at each step k: PV_k as soon as P_k is
+        // written, and S_{k+3} into the buffer PV_k has just read (after PV_k
+        // completes), so the QK^T of a tile is ready two softmax periods early.
+        for (int kn = 0; kn < kSBufs && kn < ntiles && ok; ++kn) {
           ok = s_ready(kn);
           if (!ok) break;
           tc_fence_after();
@@ -498,20 +498,16 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
           tc_commit(smem_u32(&k_empty[kn % kKStages]));
         }
         for (k = 0; k < ntiles && ok; ++k) {
-          const int kn = k + 2;
-          const bool do_s = kn < ntiles;
-          ok = wait1(smem_u32(&p_full[k % kSBufs]), (k / kSBufs) & 1, abort_flag);
-          if (ok) ok = wait1(smem_u32(&v_full[k % kVStages]), (k / kVStages) & 1, abort_flag);
-          if (ok && do_s) ok = s_ready(kn);
+          const int kn = k + kSBufs;
+          ok = wait1(smem_u32(&v_full[k % kVStages]), (k / kVStages) & 1, abort_flag);
+          if (ok) ok = wait1(smem_u32(&p_full[k % kSBufs]), (k / kSBufs) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint64_t v_desc = v_desc0 + ((uint32_t)((k % kVStages) * TILE_BYTES) >> 4);
           // PV_k: keys 0..31 -> O_A (P at S columns 0..15), keys 32..63 -> O_B
-          // (P at S columns 32..47), key blocks in the order 0, 2, 1, 3, each
-          // after one MMA of S_{k+2}
+          // (P at S columns 32..47)
 #pragma unroll
           for (int j = 0; j < kTileRows / 16; ++j) {
-            if (do_s) s_mma(kn, j);
             const int kk = (j >> 1) | ((j & 1) << 1);
             const uint64_t bdesc = v_desc + (uint32_t)((kk * 16 * 128) >> 4);
             const uint32_t o = tmem + kOCol + (kk >= 2 ? kOHalfStride : 0);
@@ -520,9 +516,12 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
           }
           tc_commit(smem_u32(&pv_done[k % kSBufs]));
           tc_commit(smem_u32(&v_empty[k % kVStages]));
-          if (do_s) {
+          if (kn < ntiles) {
+            ok = s_ready(kn);  // K_{k+3} in, PV_k (the reader of this buffer) done
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-            for (int kk = kTileRows / 16; kk < D / 16; ++kk) s_mma(kn, kk);
+            for (int kk = 0; kk < D / 16; ++kk) s_mma(kn, kk);
             tc_commit(smem_u32(&s_full[kn % kSBufs]));
             tc_commit(smem_u32(&k_empty[kn % kKStages]));
           }
@@ -578,6 +577,11 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       } else {
         t = cur.next();
       }
+      const int buf = k % kBiasBufs;
+      if (!waitw(smem_u32(&b_full[buf]), (k / kBiasBufs) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       if (!waitw(smem_u32(&s_full[k % kSBufs]), (k / kSBufs) & 1, abort_flag)) {
         ok = false;
         break;
@@ -586,11 +590,6 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       uint32_t sraw[32];
       tmem_ld32(tlane + 64 * (k % kSBufs) + c0, sraw);
       tmem_ld_wait();
-      const int buf = k % kBiasBufs;
-      if (!waitw(smem_u32(&b_full[buf]), (k / kBiasBufs) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
       // visible key columns of this row in this tile, and in my half
       int cl = max(lo_i, t.klo) - t.jbase;
       int ch = min(pi, t.khi) - t.jbase;
