@@ -35,6 +35,9 @@
 //    or two buffers in two rounds where that leaves room for a third stage)
 //    and written as the final bf16 output or, when the sequence spans several
 //    splits, as a normalised fp32 partial plus its lse for the merge kernel.
+// The kernel is launched with programmatic stream serialization: its CTAs may
+// start their set-up while the previous kernel on the stream finishes, and wait
+// (griddepcontrol) for it before reading or writing anything in global memory.
 // Reduction order depends only on logical key positions and host scalars,
 // never on page ids or on which CTA ran an item, so results are bit-identical
 // under any physical page permutation and any schedule.
@@ -236,6 +239,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
+  // launched with programmatic stream serialization: the set-up above may
+  // overlap the previous kernel on the stream; nothing it wrote is read (or
+  // overwritten) before that kernel has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // =================================================================== producer
   if (warp == kConsumerWarps) {
@@ -1082,7 +1090,17 @@ static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int sme
   static std::atomic<int> limit_set[kMaxDevices];
   if (!smem_limit_on_device(reinterpret_cast<const void*>(kern), 227 * 1024, limit_set))
     return INKLING_ERR_CUDA;
-  kern<<<grid, kDecodeThreads, smem_bytes, c.stream>>>(prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return INKLING_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return INKLING_ERR_CUDA;
   return INKLING_OK;
 }
