@@ -114,6 +114,40 @@ def test_append_then_decode_is_decode(ops):
     assert torch.equal(lse, ref_lse)
 
 
+def test_append_then_decode_back_to_back(ops):
+    """The same check at a full decode batch, twenty rounds queued on one
+    stream with no synchronisation: each round blanks the current tokens'
+    rows (a torch kernel), appends them back and decodes.  Decode may start its
+    set-up while the append is still running, so this pins that it reads the
+    cache only after the append's writes are visible."""
+    lens = torch.randint(1024, 8193, (64,), generator=torch.Generator().manual_seed(3)).tolist()
+    inp = W.make_decode(64, 48, 16, 128, 64, lens, 512, 512, device=DEV, seed=13)
+    ref_out, ref_lse = ops.decode_inputs(inp)
+    torch.cuda.synchronize()
+    B = inp.B
+    pt = inp.page_table.cpu()
+    pages = torch.tensor([int(pt[b, (L - 1) // inp.page_size]) for b, L in enumerate(lens)],
+                         device=DEV)
+    slots = torch.tensor([(L - 1) % inp.page_size for L in lens], device=DEV)
+    kc = inp.k_cache.clone()
+    vc = inp.v_cache.clone()
+    k_new = kc[pages, slots].clone()
+    v_new = vc[pages, slots].clone()
+    cu = torch.arange(B + 1, dtype=torch.int32, device=DEV)
+    outs = []
+    for _ in range(20):
+        kc[pages, slots] = float("nan")
+        vc[pages, slots] = float("nan")
+        ops.kv_append(k_new, v_new, cu, inp.seq_lens, inp.page_table, kc, vc)
+        out, lse = ops.decode(inp.q, kc, vc, inp.page_table, inp.seq_lens, inp.rel_logits,
+                              window=inp.window, scale=inp.scale, max_seq_len=inp.max_seq_len)
+        outs.append((out, lse))
+    torch.cuda.synchronize()
+    for out, lse in outs:
+        assert np.array_equal(bits(out), bits(ref_out))
+        assert torch.equal(lse, ref_lse)
+
+
 def test_bad_page_is_reported_and_skipped(ops):
     c = make_case([3, 2], [10, 20], 2, 64, 16, seed=7)
     c["pt"] = c["pt"].clone()
