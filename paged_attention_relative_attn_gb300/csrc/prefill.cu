@@ -626,8 +626,12 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&b_empty[buf]));  // band read: the loader may refill it
       if (!full_vis) {
+        // my half's visible columns as a bit mask: column cc is visible iff
+        // hl <= c0 + cc <= hh
+        const int lo = hl - c0, hi = hh - c0;
+        const uint32_t vis = lo > hi ? 0u : ((0xffffffffu >> (31 - hi)) & (0xffffffffu << lo));
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) s[cc] = (c0 + cc >= cl && c0 + cc <= ch) ? s[cc] : -INFINITY;
+        for (int cc = 0; cc < 32; ++cc) s[cc] = (vis & (1u << cc)) ? s[cc] : -INFINITY;
       }
 
       float mx;
