@@ -26,7 +26,8 @@
 //    two 8-wide n-tiles, so M is never padded), add the bias read from L2
 //    (the producer prefetches each item's rel_logits rows there; each tile's
 //    values are loaded one tile ahead), mask, and keep an online softmax per
-//    row with warp shuffles over the keys.  P goes from the accumulator layout
+//    row with warp shuffles over the keys (the row max is re-reduced only when
+//    a score exceeds the running one by more than a factor 2^8).  P goes from the accumulator layout
 //    to the B-operand layout with movmatrix.  With one n-tile the q fragments
 //    stay in registers for the whole item; with two they are read from the
 //    item's shared-memory slot (rows padded to 272 bytes, one ldmatrix per
@@ -58,6 +59,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kDecodeThreads = kConsumerThreads + 32;
 constexpr int kItemSlots = 3;
+constexpr float kMaxSlack = 8.f;  // log2 units: scores may exceed the exponent base by 2^8
 #ifndef INKLING_DECODE_CTAS_PER_SM
 #define INKLING_DECODE_CTAS_PER_SM 2
 #endif
@@ -790,15 +792,21 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       uint32_t pb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
+        // the running max (the exponent base) is re-reduced over the warp only
+        // when a score exceeds it by more than kMaxSlack (log2 units); until
+        // then p <= 2^kMaxSlack, and O and l need no rescale
         float mx0 = fmaxf(sacc[nt][0], sacc[nt][2]);
         float mx1 = fmaxf(sacc[nt][1], sacc[nt][3]);
+        float mn0 = m_run[nt][0], mn1 = m_run[nt][1];
+        if (__any_sync(0xffffffffu, mx0 > mn0 + kMaxSlack || mx1 > mn1 + kMaxSlack)) {
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          mn0 = fmaxf(mn0, mx0);
+          mn1 = fmaxf(mn1, mx1);
         }
-        const float mn0 = fmaxf(m_run[nt][0], mx0);
-        const float mn1 = fmaxf(m_run[nt][1], mx1);
         const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
         const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
         const float al0 = ex2(m_run[nt][0] - base0);
@@ -975,39 +983,68 @@ __global__ void __launch_bounds__(kDecodeThreads, kCtasPerSm)
       if (warp < 2) put(warp);
     }
     named_bar_sync(1, kConsumerThreads);
-    for (int i = tid; i < NRi * D; i += kConsumerThreads) {
-      const int h = i / D, d = i - h * D;
+    // Per row (one thread each): the common max M, each buffer's scale
+    // 2^(m_w - M), the sum Ls and the lse, which this thread stores.  The
+    // scales replace the maxima in comb_m, 1 / Ls and the output row index go
+    // to comb_l (the thread reads its row's l values before it overwrites
+    // them).
+    // MULTI, M = -inf: no key of this item is visible to the row (a split may
+    // lie wholly past a row's position): an empty result, o = 0 and lse = -inf,
+    // which the merge weighs at zero.  With one token every key of an item is
+    // visible to its rows.
+    if (tid < NRi) {
+      const int h = tid;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kCombSlots; ++w) M = fmaxf(M, comb_m[w * HP + h]);
-      float Ls = 0.f, o = 0.f;
-      // MULTI, M = -inf: no key of this item is visible to the row (a split
-      // may lie wholly past a row's position): an empty result, o = 0 and
-      // lse = -inf, which the merge weighs at zero.  With one token every key
-      // of an item is visible to its rows.
-      if (!MULTI || M > -INFINITY) {
+      float sc[kCombSlots], Ls = 0.f;
 #pragma unroll
-        for (int w = 0; w < kCombSlots; ++w) {
-          const float sc = ex2(comb_m[w * HP + h] - M);
-          Ls = fmaf(sc, comb_l[w * HP + h], Ls);
-          o = fmaf(sc, comb_o[(w * NR + h) * OP + d], o);
-        }
+      for (int w = 0; w < kCombSlots; ++w) {
+        sc[w] = (!MULTI || M > -INFINITY) ? ex2(comb_m[w * HP + h] - M) : 0.f;
+        Ls = fmaf(sc[w], comb_l[w * HP + h], Ls);
       }
       float lse;
-      if constexpr (MULTI) {
-        o = Ls > 0.f ? o / Ls : 0.f;
-        lse = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-      } else {
-        o = o / Ls;
-        lse = (M + log2f(Ls)) * kLn2;
-      }
+      if constexpr (MULTI) lse = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+      else lse = (M + log2f(Ls)) * kLn2;
       const size_t row = out_row(h);
       if (final_out) {
-        p.out[row * D + d] = __float2bfloat16(o);
-        if (d == 0 && p.lse_out) p.lse_out[row] = lse;
+        if (p.lse_out) p.lse_out[row] = lse;
       } else {
-        p.o_part[(row * S + r.split) * D + d] = o;
-        if (d == 0) p.lse_part[row * S + r.split] = lse;
+        p.lse_part[row * S + r.split] = lse;
+      }
+#pragma unroll
+      for (int w = 0; w < kCombSlots; ++w) comb_m[w * HP + h] = sc[w];
+      if constexpr (MULTI) comb_l[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+      else comb_l[h] = 1.f / Ls;
+      reinterpret_cast<int*>(comb_l)[HP + h] = (int)row;
+    }
+    named_bar_sync(1, kConsumerThreads);
+    // o = (sum_w 2^(m_w - M) O_w) * (1 / Ls), four outputs per thread at a time: all
+    // four read their buffers before any is stored (a global store between
+    // them would order every later shared-memory read after it)
+    constexpr int kOut = 4;
+    for (int i0 = 0; i0 < NRi * D; i0 += kOut * kConsumerThreads) {
+      float ov[kOut];
+      int rowv[kOut];
+#pragma unroll
+      for (int u = 0; u < kOut; ++u) {
+        int i = i0 + u * kConsumerThreads + tid;
+        i = i < NRi * D ? i : 0;
+        const int h = i / D, d = i - h * D;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombSlots; ++w) o = fmaf(comb_m[w * HP + h], comb_o[(w * NR + h) * OP + d], o);
+        ov[u] = o * comb_l[h];
+        rowv[u] = reinterpret_cast<const int*>(comb_l)[HP + h];
+      }
+#pragma unroll
+      for (int u = 0; u < kOut; ++u) {
+        const int i = i0 + u * kConsumerThreads + tid;
+        if (i >= NRi * D) break;
+        const int d = i % D;
+        const size_t row = (size_t)rowv[u];
+        if (final_out) p.out[row * D + d] = __float2bfloat16(ov[u]);
+        else p.o_part[(row * S + r.split) * D + d] = ov[u];
       }
     }
   }
