@@ -95,6 +95,14 @@ bool smem_limit_on_device(const void* kern, int bytes, std::atomic<int>* done) {
   return true;
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 152;
+  return n;
+}
+
 // ---------------------------------------------------------------- device info
 struct DevInfo {
   int ok;  // 1 = sm_103, 0 = other, -1 = query failed

@@ -1113,14 +1113,6 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
 // ---------------------------------------------------------------------------
 // Host launcher
 
-static int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    return 152;
-  return n;
-}
-
 template <int D, int NT, int BH, bool MULTI, bool COMB2 = false>
 static int launch_decode_t(const DecodeCall& c, const DecodeParams& prm, int smem_bytes, int grid) {
   auto kern = decode_kernel<D, NT, BH, MULTI, COMB2>;

@@ -22,6 +22,9 @@ constexpr int kMaxDevices = 64;
 // false when the device query or the attribute call fails.
 bool smem_limit_on_device(const void* kern, int bytes, std::atomic<int>* done);
 
+// SMs of the current device (152 when the query fails).
+int sm_count();
+
 // Validated decode call, with the split plan resolved.
 struct DecodeCall {
   const void* q;

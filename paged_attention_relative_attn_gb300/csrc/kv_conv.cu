@@ -11,8 +11,11 @@
 // by the last w-1 inputs of this call.  The convolved rows are written into
 // the paged cache at the tokens' positions (as inkling_rel_attn_kv_append).
 //
-// Grid: x = channel blocks of 8 * 64 channels, y = (sequence, segment of 64
-// new tokens), z = K or V: small CTAs, many of them, all resident at once.  A
+// Grid: x = channel blocks of 8 * 64 channels, y = (sequence, segment of
+// 32..64 new tokens), z = K or V: small CTAs, many of them, all resident at
+// once.  The launcher picks the segment length that spreads the CTAs most
+// evenly over the SMs (for 4 x 2048 tokens: 54, eight CTAs on every SM
+// rather than seven on most and six on the rest).  A
 // thread owns 8 adjacent channels (16-byte loads and stores, 512 contiguous
 // bytes per warp and token), keeps the last w-1 inputs in registers and walks
 // its segment's tokens in order.  Its input rows arrive through a private
@@ -34,7 +37,9 @@
 namespace ira {
 
 constexpr int kConvThreads = 64;
-constexpr int kConvSeg = 64;     // new tokens per CTA (>= the widest window)
+constexpr int kConvSegMin = 32;  // new tokens per CTA: 32..64 (more than the widest window)
+constexpr int kConvSegMax = 64;
+constexpr int kConvSegCost = 8;  // a CTA's fixed work, in tokens, for the segment choice
 constexpr int kConvChan = 8;     // channels per thread
 constexpr int kRingSlots = 8;    // shared-memory ring slots per thread (one token row each)
 constexpr int kRingAhead = 6;    // token rows in flight per thread
@@ -59,7 +64,7 @@ struct KvConvParams {
   const int32_t* page_table;
   const int32_t* slots;
   int32_t* dev_err;
-  int B, T, pt_stride, P, num_pages, num_slots, C8, segs;
+  int B, T, pt_stride, P, num_pages, num_slots, C8, segs, seg_len;
 };
 
 // bf16 -> fp32 is exact: the bf16 bits are the high half of the float.
@@ -94,7 +99,7 @@ __global__ void __launch_bounds__(kConvThreads)
 
   const int t0 = __ldg(p.cu + b);
   const int q_len = __ldg(p.cu + b + 1) - t0;
-  const int s0 = seg * kConvSeg;
+  const int s0 = seg * p.seg_len;
   if (q_len <= 0 || s0 >= q_len) return;
   const int L = __ldg(p.seq_lens + b);
   const int slot = NS > 0 ? __ldg(p.slots + b) : 0;
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(kConvThreads)
     if (reporter && seg == 0) report(p.dev_err, INKLING_DEVERR_BAD_SLOT);
     return;
   }
-  if (seg == p.segs - 1 && s0 + kConvSeg < q_len && reporter)
+  if (seg == p.segs - 1 && s0 + p.seg_len < q_len && reporter)
     report(p.dev_err, INKLING_DEVERR_BAD_CHUNK);  // tokens past max_q_len are not written
   if (c8 >= p.C8) return;
 
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kConvThreads)
     else win[j] = __ldcs(x + (size_t)(s0 - NS + j) * p.C8);
   }
 
-  const int s1 = min(s0 + kConvSeg, q_len);
+  const int s1 = min(s0 + p.seg_len, q_len);
   int lp = (L - q_len + s0) / p.P;             // logical page of the segment's first token
   int in_page = (L - q_len + s0) - lp * p.P;   // its slot
   size_t row0 = 0;                             // first row of the current physical page
@@ -210,9 +215,9 @@ __global__ void __launch_bounds__(kConvThreads)
   // new state: the last w-1 inputs of the sequence.  When all its new tokens
   // fall in this first segment, the window now holds exactly those (it began
   // as the old state and took every new token); otherwise they are the last
-  // w-1 new tokens (q_len > kConvSeg >= w-1).
+  // w-1 new tokens (q_len > seg_len >= w-1).
   if (seg == 0) {
-    if (q_len <= kConvSeg) {
+    if (q_len <= p.seg_len) {
 #pragma unroll
       for (int j = 0; j < NS; ++j) st[(size_t)j * p.C8] = win[j];
     } else {
@@ -244,7 +249,24 @@ int launch_kv_conv_append(const KvConvCall& c) {
   prm.num_pages = c.num_pages;
   prm.num_slots = c.num_slots;
   prm.C8 = c.H_kv * c.D / kConvChan;
-  prm.segs = (c.max_q_len + kConvSeg - 1) / kConvSeg;
+  // segment length: the fewest CTAs on the busiest SM, weighted by the
+  // tokens each walks plus its fixed work
+  {
+    const int nsm = sm_count();
+    const int64_t cblocks = (prm.C8 + kConvThreads - 1) / kConvThreads;
+    int64_t best = -1;
+    prm.seg_len = kConvSegMax;
+    for (int len = kConvSegMax; len >= kConvSegMin; --len) {
+      const int64_t segs = (c.max_q_len + len - 1) / len;
+      const int64_t ctas = 2 * cblocks * (int64_t)c.B * segs;
+      const int64_t cost = (ctas + nsm - 1) / nsm * (len + kConvSegCost);
+      if (best < 0 || cost < best) {
+        best = cost;
+        prm.seg_len = len;
+      }
+    }
+  }
+  prm.segs = (c.max_q_len + prm.seg_len - 1) / prm.seg_len;
   const int64_t gy = (int64_t)c.B * prm.segs;  // (sequence, segment) pairs
   if (gy <= 0 || gy > 65535) return INKLING_ERR_ARG;
   const dim3 grid((prm.C8 + kConvThreads - 1) / kConvThreads, (unsigned)gy, 2);
