@@ -101,7 +101,7 @@ CASES = [
     # q_lens, kv_lens, H_kv, D, P, width
     ([1, 1, 1], [9, 64, 200], 2, 64, 16, 4),           # decode steps
     ([1, 5, 70], [9, 64, 200], 8, 128, 64, 4),         # mixed chunks; a token shorter than the window
-    ([2, 1, 150], [40, 7, 400], 4, 128, 16, 8),        # chunks shorter than the window; 3 segments
+    ([2, 1, 150], [40, 7, 400], 4, 128, 16, 8),        # chunks shorter than the window; several segments
     ([16, 0, 33], [16, 7, 100], 16, 128, 64, 3),       # a whole first page; an idle sequence
     ([3, 65, 1], [3, 65, 20], 2, 64, 16, 2),           # a request's first tokens
     ([128], [4000], 8, 128, 64, 4),                    # a chunk far into a long sequence
