@@ -258,6 +258,7 @@ int launch_kv_conv_append(const KvConvCall& c) {
     prm.seg_len = kConvSegMax;
     for (int len = kConvSegMax; len >= kConvSegMin; --len) {
       const int64_t segs = (c.max_q_len + len - 1) / len;
+      if (len < kConvSegMax && (int64_t)c.B * segs > 65535) break;  // grid y limit: keep longer segments
       const int64_t ctas = 2 * cblocks * (int64_t)c.B * segs;
       const int64_t cost = (ctas + nsm - 1) / nsm * (len + kConvSegCost);
       if (best < 0 || cost < best) {
