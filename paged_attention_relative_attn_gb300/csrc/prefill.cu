@@ -6,7 +6,9 @@
 // applying the relative bias to the scores; "Architecture": bias per (query
 // token, head, relative distance), sliding window 512 / full causal).
 //
-// One CTA per (128-query tile of one sequence, query head), 12 warps:
+// One CTA per (128-query tile of one sequence, query head; a sequence's
+// tiles launch last tile first, the longest key ranges ahead of the shortest),
+// 12 warps:
 //  * warp 0 loads the Q tile once (TMA) and then the K tiles of the tile's
 //    visible key range into a 3-stage ring, in page-respecting tiles of 64
 //    keys exactly like the decode kernel; warp 6 loads the V tiles the same
@@ -233,7 +235,9 @@ __global__ void __launch_bounds__(kPrefThreads, 1)
   const int lane = tid & 31;
   const int h = blockIdx.x;
   const int b = blockIdx.y / p.tiles_per_seq;
-  const int qt = blockIdx.y - b * p.tiles_per_seq;
+  // a sequence's query tiles run last tile first: later tiles see more keys,
+  // so a call ends on its shortest CTAs
+  const int qt = p.tiles_per_seq - 1 - (int)(blockIdx.y - b * p.tiles_per_seq);
   if (b >= p.B) return;
 
   // ---- the sequence's scalars, loaded together; their latency overlaps the
