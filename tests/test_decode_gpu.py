@@ -189,6 +189,25 @@ def test_one_hot_bias_bit_exact(ops, kind):
                 assert torch.equal(out[b, h], want), (kind, d, b, h)
 
 
+@pytest.mark.parametrize("slope", [0.05, 0.3])
+def test_rising_bias(ops, slope):
+    """A bias that grows toward the most recent keys (rel = -slope * distance)
+    raises every row's max along the key walk: by about 4.6 (slope 0.05) or
+    28 (slope 0.3) log2 units per 64-key tile, so the exponent base, which is
+    re-reduced only when a score passes it by more than 2^8, and the O rescale
+    are taken every one to two tiles."""
+    import dataclasses
+    lens = [700, 1000, 129, 64]
+    inp = W.make_decode(4, 48, 8, 128, 64, lens, 0, 1024, device=DEV, seed=21, poison=True)
+    d = torch.arange(inp.R, device=DEV, dtype=torch.float32)
+    rel = (-slope * d).expand_as(inp.rel_logits).contiguous()
+    inp2 = dataclasses.replace(inp, rel_logits=rel)
+    for splits in (1, 4):
+        out, lse = run(ops, inp2, num_splits=splits)
+        ro, rl = oracle_decode(inp2)
+        assert_close(out, ro, lse, rl, what=f"slope {slope}, {splits} splits")
+
+
 def test_single_visible_key_bit_exact(ops):
     lens = [1, 2, 64, 65, 1000]
     inp = W.make_decode(5, 48, 16, 128, 64, lens, 1, 512, device=DEV, seed=13, poison=True,

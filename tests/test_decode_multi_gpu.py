@@ -87,6 +87,23 @@ def test_forced_splits_six_rows(ops, case, splits):
     assert_close(out, ro, lse, rl, what=f"case {case}, {splits} splits")
 
 
+@pytest.mark.parametrize("slope", [0.05, 0.3])
+def test_rising_bias(ops, slope):
+    """rel = -slope * distance: every row's max rises along the key walk, so
+    the lazily re-reduced exponent base and the O rescale are taken every one
+    to two tiles (two n-tiles: 4 tokens x 3 heads per item)."""
+    import dataclasses
+    lens, ql = [700, 1000, 129, 64], 4
+    inp = make(lens, ql, 12, 4, 128, 64, 512, 512, seed=390)
+    d = torch.arange(inp.R, device=DEV, dtype=torch.float32)
+    rel = (-slope * d).expand_as(inp.rel_logits).contiguous()
+    inp2 = dataclasses.replace(inp, rel_logits=rel)
+    out, lse, err = run(ops, inp2, ql)
+    assert err == 0
+    ro, rl, tok = oracle_prefill(inp2)
+    assert_close(out, ro, lse, rl, what=f"slope {slope}")
+
+
 def test_one_token_is_decode_bit_exact(ops):
     inp = W.make_decode(6, 48, 16, 128, 64, [1, 63, 64, 65, 700, 3000], 512, 512, device=DEV,
                         seed=21)

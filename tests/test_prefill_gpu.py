@@ -63,6 +63,23 @@ def test_small_cases(ops, case, q_std):
     assert_close(out.index_select(0, idx), ro, lse.index_select(0, idx), rl, what=f"case {case}")
 
 
+@pytest.mark.parametrize("slope", [0.05, 0.3])
+def test_rising_bias(ops, slope):
+    """rel = -slope * distance: every row's max rises along the key walk, by
+    about 4.6 or 28 log2 units per 64-key tile, so the lazy O rescale (taken
+    when a row's max passes the exponent base by more than 2^8) runs every one
+    to two tiles, each time after waiting for the pending PV."""
+    import dataclasses
+    inp = make([300, 129], [1000, 400], 6, 2, 128, 64, 0, 1024, seed=260)
+    d = torch.arange(inp.R, device=DEV, dtype=torch.float32)
+    rel = (-slope * d).expand_as(inp.rel_logits).contiguous()
+    inp2 = dataclasses.replace(inp, rel_logits=rel)
+    out, lse = run(ops, inp2)
+    ro, rl, rows = oracle_prefill(inp2)
+    idx = torch.tensor(rows, dtype=torch.long, device=DEV)
+    assert_close(out.index_select(0, idx), ro, lse.index_select(0, idx), rl, what=f"slope {slope}")
+
+
 def oracle_rows(inp, rows_by_seq):
     """Oracle for selected query rows: row i of sequence b (q_len Q, L keys) is
     the decode query at position L - Q + i over the sequence cut there."""
